@@ -1,0 +1,415 @@
+"""Decode-step benchmark: paged decode attention HBM GB/s on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload l3-70b] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch: reshape_and_cache of
+the step's new tokens, copy_blocks of its copy-on-write pairs (prefix
+workloads only), then paged_attention_decode.  ``value`` is the step's useful
+bytes (attended K/V + Q + O + appended K/V read and written + copied blocks)
+over its device time, all inputs resident in HBM.  ``e2e`` is the same metric
+through the public API with per-step inputs (q, new K/V, slots, tables,
+lengths) copied from pinned host memory and the output copied back inside the
+timed region; the KV cache itself stays resident, as it does in serving.
+
+Multi-GPU: decode shards by sequence with no exchange, so each rank runs its
+own batch (seed + rank); ``value`` sums all ranks' bytes over the slowest
+rank's time (weak scaling).  ``--impl reference`` times the float64 CPU oracle
+on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn achieved HBM GB/s & % of GB300 peak; decode tokens/s per layer"
+WORKLOAD_DESC = {
+    "l3-70b": "Llama-3-70B-shaped serving batch: 256 seqs, 64 q / 8 kv heads (GQA 8), head_dim 128, "
+              "block_size 16, seq_lens lognormal(median 600, sigma 1) clipped to [16, 8192] + 1 appended "
+              "token each, shuffled pool (needed + 10%)",
+    "l3-8b": "Llama-3-8B-shaped decode layer: 64 seqs, 32 q / 8 kv heads, head_dim 128, block_size 16, "
+             "seq_lens U[512, 2048]",
+    "long": "Long-context split-K: 8 seqs, 32 q / 8 kv heads, head_dim 128, block_size 16, seq_lens U[32768, 131072]",
+    "tiny": "Tiny: 4 seqs, 8 q / 8 kv heads, head_dim 64, block_size 16, seq_lens U[1, 128] + 1",
+    "prefix-b8": "Prefix sharing + CoW, block_size 8",
+    "prefix-b16": "Prefix sharing + CoW, block_size 16",
+    "prefix-b32": "Prefix sharing + CoW, block_size 32",
+}
+# Kernel source files whose change invalidates the recorded ncu traffic.
+DOMINANT_SOURCES = ["paged_kv_cache_122_gb300/csrc/decode_cuda_core.cu", "paged_kv_cache_122_gb300/csrc/decode_api.cu",
+                    "paged_kv_cache_122_gb300/csrc/decode.cuh"]
+# DRAM bytes per launch of the dominant kernel from one ncu capture, and the
+# hash of its sources at that time (profiles/ holds the summary).
+RECORDED_TRAFFIC = {"sources_sha1": None, "bytes_per_launch": None, "workload": "l3-70b"}
+
+
+def sources_sha1() -> str:
+    h = hashlib.sha1()
+    for rel in DOMINANT_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+CPU_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+try:
+    os.sched_setaffinity(0, {{sorted(os.sched_getaffinity(0))[0]}})
+except Exception:
+    pass
+import oracle
+from paged_kv_cache_122_gb300 import workloads as W, metrics as M
+w = W.get({workload!r}, {seed})
+sel = list(range(min({nseq}, w.num_seqs)))
+wc = W.custom({seed}, w.seq_lens[sel], w.num_heads, w.num_kv_heads, w.head_dim, w.block_size)
+t = W.make_tensors(wc, "cpu")
+q, kc, vc = (W.bits(t[k]) for k in ("q", "k_cache", "v_cache"))
+nbytes = M.useful_bytes(wc)["attention"]
+times = []
+t_end = time.perf_counter() + {budget}
+while True:
+    t0 = time.perf_counter()
+    oracle.paged_decode_attention(q, kc, vc, wc.block_tables, wc.seq_lens, wc.scale, wc.block_size)
+    times.append(time.perf_counter() - t0)
+    if time.perf_counter() > t_end or len(times) >= {max_reps}:
+        break
+print(json.dumps({{"times": times, "bytes": nbytes, "seqs": len(sel), "tokens": int(wc.seq_lens.sum())}}))
+"""
+
+
+def run_cpu_oracle(workload: str, seed: int, nseq: int, budget_s: float, max_reps: int = 1000):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = CPU_SNIPPET.format(root=ROOT, workload=workload, seed=seed, nseq=nseq, budget=budget_s,
+                              max_reps=max_reps)
+    cmd = [sys.executable, "-c", code]
+    res = subprocess.run(cmd, capture_output=True, text=True, env=env)
+    if res.returncode != 0:
+        raise RuntimeError(f"CPU oracle run failed:\n{res.stderr[-2000:]}")
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch
+    import paged_kv_cache_122_gb300 as pk
+    from paged_kv_cache_122_gb300 import metrics as M, workloads as W
+
+    ws, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk.load_library()
+    w = W.get(args.workload, args.seed + rank)
+    t = W.make_tensors(w, dev)
+    ub = M.useful_bytes(w)
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    ws_bytes = pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.max_seq_len)
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)       # 2x the 129 MB L2
+
+    def attend(o=out, q=t["q"], bt=t["block_tables"], sl=t["seq_lens"]):
+        pk.pk_paged_attention_decode(o, q, t["k_cache"], t["v_cache"], bt, sl, w.scale, w.block_size,
+                                     w.max_seq_len, workspace)
+
+    def prelude(kn=t["k_new"], vn=t["v_new"], sm=t["slot_mapping"]):
+        if w.copy_pairs.shape[0]:
+            pk.copy_blocks(t["k_cache"], t["v_cache"], t["copy_pairs"])
+        if w.num_new_tokens:
+            pk.reshape_and_cache(kn, vn, t["k_cache"], t["v_cache"], sm)
+
+    launches_per_step = (1 if w.copy_pairs.shape[0] else 0) + (1 if w.num_new_tokens else 0) + 1 + \
+        (1 if w.max_seq_len > 512 else 0)
+
+    for _ in range(args.warmup):
+        prelude()
+        attend()
+    torch.cuda.synchronize(dev)
+    assert pk.pk_get_device_error(dev) == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()                                     # evict L2 between steps (outside the events)
+            ev[i][0].record(stream)
+            prelude()
+            ev[i][1].record(stream)
+            attend()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            torch.distributed.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(step_ms)
+
+    # End to end through the public API with host buffers.
+    host = {k: t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")}
+    dbuf = {k: torch.empty_like(t[k]) for k in host}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        prelude(dbuf["k_new"], dbuf["v_new"], dbuf["slot_mapping"])
+        attend(out, dbuf["q"], dbuf["block_tables"], dbuf["seq_lens"])
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    assert pk.pk_get_device_error(dev) == 0
+
+    if ws > 1:
+        import torch.distributed as dist
+        vals = torch.tensor([total_ms, e2e_ms, float(ub["step"])], dtype=torch.float64, device=dev)
+        mx = vals.clone()
+        dist.all_reduce(mx[:2], op=dist.ReduceOp.MAX)
+        sm = vals.clone()
+        dist.all_reduce(sm[2:], op=dist.ReduceOp.SUM)
+        total_ms, e2e_ms, all_bytes = float(mx[0]), float(mx[1]), float(sm[2])
+    else:
+        all_bytes = float(ub["step"])
+
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    ms_per_step = total_ms / args.steps
+    value = all_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    attn_gbs = ub["attention"] / (attn_avg_ms * 1e-3) / 1e9
+    traffic = None
+    if RECORDED_TRAFFIC["sources_sha1"] == sources_sha1() and RECORDED_TRAFFIC["workload"] == args.workload:
+        traffic = RECORDED_TRAFFIC["bytes_per_launch"]
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}",
+            "num_seqs": w.num_seqs, "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "tokens_attended": ub["tokens"], "new_tokens": w.num_new_tokens,
+            "copy_pairs": int(w.copy_pairs.shape[0]), "seed": args.seed,
+            "useful_bytes_per_step": ub["step"], "attention_bytes": ub["attention"],
+            "unique_kv_bytes": ub["kv_unique"],
+            "l2": "flushed between timed steps (256 MiB write outside the events); K/V inputs also exceed L2",
+            "parallelism": f"replicas x{ws} (independent batches, no collective)",
+        },
+        "pct_of_peak": round(100.0 * value / peak, 2),
+        "tokens_per_s_per_layer": round(w.num_seqs * ws / (ms_per_step * 1e-3), 1),
+        "roofline": {
+            "kernel": "paged_attention_decode",
+            "bound": "hbm",
+            "achieved": round(attn_gbs, 2),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": round(attn_gbs / peak, 4),
+            "traffic": traffic,
+            "avg_launch_ms": round(attn_avg_ms, 5),
+            "algorithmic_bytes_per_launch": ub["attention"],
+        },
+        "e2e": {
+            "value": round(all_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms / args.steps, 5),
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        r = run_cpu_oracle(args.workload, args.seed, args.cpu_seqs, args.cpu_budget)
+        tot = sum(r["times"])
+        res["cpu_baseline"] = {
+            "value": round(r["bytes"] * len(r["times"]) / tot / 1e9, 4),
+            "unit": "GB/s",
+            "cores": 1,
+            "kind": "oracle",
+            "sample": f"float64 oracle decode attention over the first {r['seqs']} sequences "
+                      f"({r['tokens']} tokens) of the same workload, {len(r['times'])} passes, "
+                      f"{tot:.1f} s on one pinned host core",
+        }
+    return res
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    # Each step: the oracle over a bounded sample of the workload (first
+    # --ref-seqs sequences); warm-up passes are discarded.
+    r = run_cpu_oracle(args.workload, args.seed, args.ref_seqs, budget_s=1e9,
+                       max_reps=args.steps + args.warmup)
+    times = r["times"][args.warmup:] or r["times"]
+    tot = sum(times)
+    value = r["bytes"] * len(times) / tot / 1e9
+    sample = (f"float64 oracle decode attention over the first {r['seqs']} sequences ({r['tokens']} tokens) "
+              f"of the workload per step, one pinned host core")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": len(times),
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot / len(times), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}", "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="l3-70b", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seqs", type=int, default=256)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-seqs", type=int, default=32)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

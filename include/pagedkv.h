@@ -1,0 +1,209 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode path.
+ *
+ * Three operations make up one decode step of PagedAttention:
+ *
+ *   pk_copy_blocks            copy-on-write clones of shared blocks
+ *   pk_reshape_and_cache      append each new token's K/V to its slot
+ *   pk_paged_attention_decode single-query attention through block tables
+ *
+ * plus helpers (workspace sizing, a block-table gather used to check the
+ * table walk bit for bit, the device error word, status strings).
+ *
+ * Conventions common to every call
+ * --------------------------------
+ * Pointers.  Every tensor argument is a DEVICE pointer into memory the caller
+ *   allocated and owns (cudaMalloc, a torch tensor, a pool).  The library keeps
+ *   no pointer after a call returns and allocates no device memory.  All
+ *   tensors are dense, row-major, with the shapes given below.
+ * Types.  K/V/Q/new-token tensors are bf16 (IEEE binary32 truncated to its top
+ *   16 bits, passed as raw 16-bit words).  block_tables and seq_lens are int32;
+ *   slot_mapping and copy pairs are int64.
+ * Cache layout.  k_cache and v_cache are [num_blocks, block_size, num_kv_heads,
+ *   head_dim]: the tokens of a block side by side, the heads of a token side by
+ *   side, the elements of a head side by side ("PagedAttention from First
+ *   Principles", §7 "Inside the attention kernel"; "vLLM — PagedAttention",
+ *   "Fused CUDA Kernels", conceptual kernel signature).
+ * Streams.  Every call is enqueued on `stream` (NULL = the legacy default
+ *   stream) and returns without waiting for the GPU, except
+ *   pk_get_device_error, which synchronises `stream`.  No call reads device
+ *   memory from the host, so the three step calls can be captured in a graph.
+ * Alignment.  Device pointers must be 16-byte aligned (cudaMalloc and torch
+ *   give 256); head_dim*2 bytes is then a multiple of 16 for every supported
+ *   head_dim, so every row the kernels move is 16-byte aligned too.
+ * Errors.  A call first checks its arguments on the host and returns a
+ *   negative pk_status without launching anything if one is bad.  A failed
+ *   launch returns PK_ERR_CUDA.  Bad DATA in device memory (a block id outside
+ *   the pool, a slot past the pool, a length longer than the table) cannot be
+ *   seen from the host: the kernels skip that access, never fault or trap, and
+ *   OR a PK_DEVERR_* bit into a per-device error word that
+ *   pk_get_device_error reads and clears.
+ * Supported sizes.  head_dim in {64, 128}; block_size in {8, 16, 32};
+ *   num_heads a multiple of num_kv_heads with G = num_heads / num_kv_heads in
+ *   {1, 2, 4, 8, 16}; num_kv_heads >= 1.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *pk_stream_t;
+
+enum pk_status {
+    PK_OK = 0,
+    PK_ERR_NULL = -1,          /* a required pointer is NULL */
+    PK_ERR_SHAPE = -2,         /* sizes inconsistent or out of range */
+    PK_ERR_UNSUPPORTED = -3,   /* head_dim, block_size or group size not supported */
+    PK_ERR_WORKSPACE = -4,     /* workspace missing or smaller than required */
+    PK_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
+    PK_ERR_ALIGNMENT = -6,     /* a pointer is not 16-byte aligned */
+    PK_ERR_NO_DEVICE = -7      /* no usable CUDA device */
+};
+
+enum pk_dtype { PK_BF16 = 0, PK_FP32 = 1 };
+
+/* Bits of the device error word. */
+#define PK_DEVERR_BLOCK_ID 0x1u /* a table entry below ceil(L/B) is outside [0, num_blocks) */
+#define PK_DEVERR_SLOT     0x2u /* a slot_mapping entry is >= num_blocks * block_size */
+#define PK_DEVERR_PAIR     0x4u /* a copy pair names a block outside [0, num_blocks) */
+#define PK_DEVERR_SEQ_LEN  0x8u /* a seq_len is negative, exceeds max_seq_len or exceeds
+                                   max_blocks_per_seq * block_size */
+
+/* Human-readable name of a pk_status value; never NULL. */
+const char *pk_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int pk_version(void);
+
+/*
+ * Bytes of workspace pk_paged_attention_decode needs for these sizes.
+ *
+ * The workspace holds the split-K partial results of long sequences: for every
+ * (sequence, KV head, partition) the running max and denominator of each of the
+ * G query heads and their unnormalised output rows, all fp32.  It is sized for
+ * the worst case the host can see (every sequence as long as max_seq_len), so
+ * the call never needs to read seq_lens on the host.  Returns 0 for invalid
+ * sizes.
+ */
+size_t pk_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int max_seq_len);
+
+/*
+ * Single-query decode attention over a paged KV cache.
+ *
+ * Defined by "vLLM — PagedAttention", Mathematical Formulation (Equation 4):
+ * for sequence s of length L = seq_lens[s] and query head h,
+ *
+ *   out[s,h,:] = sum_j softmax_j(scale * q[s,h,:] . k_j) v_j,  j = 0 .. L-1,
+ *
+ * where token j lives in physical block block_tables[s, j / B] at offset j % B
+ * ("PagedAttention from First Principles", §5: the kernel reads every block
+ * through the table) and k_j, v_j are the rows of KV head h / G.  Table entries
+ * at or beyond ceil(L/B) are never read, whatever they hold (§6: the sentinel
+ * of unused table slots is never dereferenced).  L = 0 writes zeros.
+ *
+ *   out           [num_seqs, num_heads, head_dim], bf16 (out_dtype PK_BF16,
+ *                 round-to-nearest-even of the fp32 result) or fp32 (PK_FP32)
+ *   q             [num_seqs, num_heads, head_dim] bf16
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, num_kv_heads, head_dim] bf16
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32
+ *   seq_lens      [num_seqs] int32, each in [0, max_seq_len]
+ *   max_seq_len   host-side upper bound of seq_lens, used only to size the
+ *                 split-K plan; must be <= max_blocks_per_seq * block_size.
+ *                 A device length above it sets PK_DEVERR_SEQ_LEN and only its
+ *                 first max_seq_len tokens are attended.
+ *   scale         multiplies q.k before the softmax (1/sqrt(head_dim) for the
+ *                 usual attention)
+ *   workspace     device scratch of at least pk_decode_workspace_bytes(...)
+ *                 bytes; its contents on entry do not matter.  Calls that share
+ *                 one workspace must be ordered on the GPU (same stream).
+ *
+ * Long sequences are split into partitions processed in parallel and combined
+ * by a log-sum-exp merge ("PagedAttention from First Principles", §17: the
+ * partitioned kernel and its reduce step).  Results do not depend on the
+ * physical placement of blocks and are deterministic run to run.
+ */
+int pk_paged_attention_decode(void *out, int out_dtype, const void *q,
+                              const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, int max_seq_len,
+                              int num_seqs, int num_heads, int num_kv_heads,
+                              int head_dim, int num_blocks, int block_size,
+                              float scale, void *workspace, size_t workspace_bytes,
+                              pk_stream_t stream);
+
+/*
+ * Append new tokens' K/V to their cache slots ("vLLM — PagedAttention",
+ * Fused CUDA Kernels (1), fused reshape and block write; "PagedAttention from
+ * First Principles", §2: the cache is append-only).
+ *
+ *   k, v          [num_tokens, num_kv_heads, head_dim] bf16
+ *   slot_mapping  [num_tokens] int64: token t goes to block slot / block_size,
+ *                 offset slot % block_size, all heads.  A negative slot is a
+ *                 padding token and writes nothing.  A slot at or beyond
+ *                 num_blocks * block_size sets PK_DEVERR_SLOT and writes nothing.
+ *                 Two tokens with the same slot race (the caller never does this).
+ *
+ * num_tokens == 0 is a no-op.  Bit-exact: the cache rows become the input bits.
+ */
+int pk_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int num_tokens,
+                         int num_kv_heads, int head_dim, int num_blocks,
+                         int block_size, pk_stream_t stream);
+
+/*
+ * Copy whole blocks, K and V, one launch for all pairs ("vLLM —
+ * PagedAttention", Copy-on-Write Logic and Fused CUDA Kernels (3): batched
+ * block copies for copy-on-write).
+ *
+ *   src_dst_pairs [num_pairs, 2] int64 device array of (src, dst) block ids.
+ *                 No dst may appear twice and no dst may be the src of another
+ *                 pair (a copy-on-write step never produces that); otherwise
+ *                 the result is unspecified.  An id outside [0, num_blocks)
+ *                 sets PK_DEVERR_PAIR and that pair is skipped.
+ *
+ * num_pairs == 0 is a no-op.  Bit-exact.
+ */
+int pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
+                   int num_pairs, int num_kv_heads, int head_dim, int num_blocks,
+                   int block_size, pk_stream_t stream);
+
+/*
+ * Gather every sequence's K/V through its block table into contiguous rows:
+ * out_k[cu_seq_lens[s] + j] = k_cache[block_tables[s, j / B], j % B] for
+ * j < seq_lens[s] (same for V).  This is the table walk of the attention kernel
+ * on its own ("PagedAttention from First Principles", §5), exported so that it
+ * can be checked bit for bit.
+ *
+ *   out_k, out_v  [total_tokens, num_kv_heads, head_dim] bf16
+ *   cu_seq_lens   [num_seqs] int64 device array: first output row of each sequence
+ *   max_seq_len   host-side bound of seq_lens (as for the attention call)
+ *
+ * A table entry outside the pool sets PK_DEVERR_BLOCK_ID and its rows are left
+ * unwritten.
+ */
+int pk_gather_kv(void *out_k, void *out_v, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, int max_blocks_per_seq,
+                 const int32_t *seq_lens, const int64_t *cu_seq_lens, int max_seq_len,
+                 int num_seqs, int num_kv_heads, int head_dim, int num_blocks,
+                 int block_size, pk_stream_t stream);
+
+/*
+ * Read and clear the error word of the current device.  Synchronises `stream`
+ * first, so it reports every kernel enqueued before it on that stream.
+ * *code_out receives the OR of the PK_DEVERR_* bits set since the last clear.
+ */
+int pk_get_device_error(unsigned int *code_out, pk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

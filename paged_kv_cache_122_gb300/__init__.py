@@ -1,0 +1,24 @@
+"""GB300-native paged KV-cache decode path: a C-ABI CUDA library and its binding.
+
+The calls follow the pages' statement of the problem:
+
+* ``paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size)``
+* ``reshape_and_cache(k, v, k_cache, v_cache, slot_mapping)``
+* ``copy_blocks(k_cache, v_cache, src_dst_pairs)``
+
+All work runs in the library's sm_103a kernels (``csrc/``); PyTorch supplies
+device memory and streams.  Importing the package does not load the library;
+the first call does, and fails loudly if it has not been built.
+"""
+from .api import (  # noqa: F401
+    copy_blocks,
+    paged_attention_decode,
+    pk_copy_blocks,
+    pk_decode_workspace_bytes,
+    pk_gather_kv,
+    pk_get_device_error,
+    pk_paged_attention_decode,
+    pk_reshape_and_cache,
+    reshape_and_cache,
+)
+from ._native import PagedKVError, load as load_library  # noqa: F401

@@ -1,0 +1,84 @@
+"""ctypes declarations of the C ABI in ``include/pagedkv.h``.
+
+Loading fails loudly when the compiled library is missing: there is no CPU
+fallback for any operation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+c_int, c_float, c_size_t, c_void_p, c_uint = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_uint
+
+# name -> (restype, argtypes), in the header's order.
+SIGNATURES = {
+    "pk_status_string": (ctypes.c_char_p, [c_int]),
+    "pk_version": (c_int, []),
+    "pk_decode_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "pk_paged_attention_decode": (c_int, [
+        c_void_p, c_int, c_void_p,             # out, out_dtype, q
+        c_void_p, c_void_p,                    # k_cache, v_cache
+        c_void_p, c_int,                       # block_tables, max_blocks_per_seq
+        c_void_p, c_int,                       # seq_lens, max_seq_len
+        c_int, c_int, c_int, c_int,            # num_seqs, num_heads, num_kv_heads, head_dim
+        c_int, c_int, c_float,                 # num_blocks, block_size, scale
+        c_void_p, c_size_t, c_void_p]),        # workspace, workspace_bytes, stream
+    "pk_reshape_and_cache": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+        c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "pk_copy_blocks": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "pk_gather_kv": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_void_p,
+        c_void_p, c_int, c_void_p, c_void_p, c_int,
+        c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "pk_get_device_error": (c_int, [ctypes.POINTER(c_uint), c_void_p]),
+}
+
+PK_OK = 0
+PK_BF16, PK_FP32 = 0, 1
+STATUS_NAMES = {
+    0: "PK_OK", -1: "PK_ERR_NULL", -2: "PK_ERR_SHAPE", -3: "PK_ERR_UNSUPPORTED",
+    -4: "PK_ERR_WORKSPACE", -5: "PK_ERR_CUDA", -6: "PK_ERR_ALIGNMENT", -7: "PK_ERR_NO_DEVICE",
+}
+DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_SEQ_LEN = 0x1, 0x2, 0x4, 0x8
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIBPATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (once) and declare the library."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise ImportError(
+            f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()'); "
+            "this package has no CPU fallback")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = load().pk_status_string(status).decode()
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)} ({msg})")
+
+
+def check(fn: str, status: int) -> None:
+    if status != PK_OK:
+        raise PagedKVError(fn, status)

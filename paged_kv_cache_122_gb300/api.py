@@ -1,0 +1,198 @@
+"""Torch-facing binding of the C ABI: checks tensors, passes pointers.
+
+Every function here only marshals arguments (shapes, dtypes, device pointers,
+the current CUDA stream) into one C call; all work runs in the library's CUDA
+kernels.  Names follow the C entry points (``pk_*``); the unprefixed names are
+the pages' spelling of the same calls.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native
+from ._native import check, load
+
+_WORKSPACES = {}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _stream(device: torch.device, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def pk_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                              max_seq_len: int) -> int:
+    return int(load().pk_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len))
+
+
+def workspace_for(device: torch.device, nbytes: int, stream=None) -> Optional[torch.Tensor]:
+    """A cached scratch buffer of at least ``nbytes`` for ``device`` and stream."""
+    if nbytes == 0:
+        return None
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device, s.cuda_stream)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
+def pk_paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                              v_cache: torch.Tensor, block_tables: torch.Tensor,
+                              seq_lens: torch.Tensor, scale: float, block_size: Optional[int] = None,
+                              max_seq_len: Optional[int] = None,
+                              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode attention into ``out`` ([N, H, D], bf16 or fp32).  See the C header."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    _need(out, "out", out.dtype, 3, dev)
+    N, H, D = q.shape
+    P, B, Hkv, Dk = k_cache.shape
+    if block_size is not None and block_size != B:
+        raise ValueError(f"block_size {block_size} does not match the cache's {B}")
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or Dk != D:
+        raise ValueError("k_cache / v_cache / q shapes disagree")
+    if tuple(out.shape) != (N, H, D) or block_tables.shape[0] != N or seq_lens.shape[0] != N:
+        raise ValueError("out / block_tables / seq_lens do not match q's batch")
+    MB = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = MB * B
+    ws_bytes = pk_decode_workspace_bytes(N, H, Hkv, D, max_seq_len)
+    if workspace is None:
+        workspace = workspace_for(dev, ws_bytes, stream)
+    elif workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError("workspace too small")
+    with torch.cuda.device(dev):
+        st = load().pk_paged_attention_decode(
+            _ptr(out), _native.PK_FP32 if out.dtype == torch.float32 else _native.PK_BF16, _ptr(q),
+            _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), MB, _ptr(seq_lens), int(max_seq_len),
+            N, H, Hkv, D, P, B, float(scale), _ptr(workspace),
+            0 if workspace is None else workspace.numel() * workspace.element_size(),
+            _stream(dev, stream))
+    check("pk_paged_attention_decode", st)
+    return out
+
+
+def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                           block_size: Optional[int] = None, *, out_dtype=torch.bfloat16,
+                           max_seq_len: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """``paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size)``."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    return pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                                     block_size, max_seq_len, workspace, stream)
+
+
+def pk_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write new tokens' K/V ([T, Hkv, D] bf16) to their int64 slots.  See the C header."""
+    dev = k_cache.device
+    _need(k, "k", torch.bfloat16, 3, dev)
+    _need(v, "v", torch.bfloat16, 3, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    T, Hkv, D = k.shape
+    P, B, Hc, Dc = k_cache.shape
+    if tuple(v.shape) != (T, Hkv, D) or (Hc, Dc) != (Hkv, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k / v / cache shapes disagree")
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping must have one entry per token")
+    with torch.cuda.device(dev):
+        st = load().pk_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                                         T, Hkv, D, P, B, _stream(dev, stream))
+    check("pk_reshape_and_cache", st)
+
+
+reshape_and_cache = pk_reshape_and_cache
+
+
+def pk_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: torch.Tensor,
+                   stream=None) -> None:
+    """Copy whole blocks for every (src, dst) row of an int64 [n, 2] tensor.  See the C header."""
+    dev = k_cache.device
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(src_dst_pairs, "src_dst_pairs", torch.int64, 2, dev)
+    if src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [n, 2]")
+    P, B, Hkv, D = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache shapes disagree")
+    with torch.cuda.device(dev):
+        st = load().pk_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs),
+                                   src_dst_pairs.shape[0], Hkv, D, P, B, _stream(dev, stream))
+    check("pk_copy_blocks", st)
+
+
+copy_blocks = pk_copy_blocks
+
+
+def pk_gather_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                 seq_lens: torch.Tensor, seq_lens_host, max_seq_len: Optional[int] = None,
+                 stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Contiguous [sum L, Hkv, D] K and V gathered through the tables, and row offsets."""
+    dev = k_cache.device
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    P, B, Hkv, D = k_cache.shape
+    N, MB = block_tables.shape
+    lens = [int(x) for x in seq_lens_host]
+    cu = [0]
+    for L in lens[:-1]:
+        cu.append(cu[-1] + L)
+    total = sum(lens)
+    cu_t = torch.tensor(cu, dtype=torch.int64, device=dev)
+    out_k = torch.empty((max(total, 1), Hkv, D), dtype=torch.bfloat16, device=dev)
+    out_v = torch.empty_like(out_k)
+    if max_seq_len is None:
+        max_seq_len = max(lens) if lens else 0
+    with torch.cuda.device(dev):
+        st = load().pk_gather_kv(_ptr(out_k), _ptr(out_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), MB,
+                                 _ptr(seq_lens), _ptr(cu_t), int(max_seq_len), N, Hkv, D, P, B,
+                                 _stream(dev, stream))
+    check("pk_gather_kv", st)
+    return out_k[:total], out_v[:total], cu_t
+
+
+def pk_get_device_error(device=None, stream=None) -> int:
+    """Read and clear the device error word (synchronises the stream)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    code = ctypes.c_uint(0)
+    with torch.cuda.device(dev):
+        st = load().pk_get_device_error(ctypes.byref(code), _stream(dev, stream))
+    check("pk_get_device_error", st)
+    return int(code.value)

@@ -1,0 +1,190 @@
+// Cache writes, block copies and the table-walk gather.
+//
+// All three are byte movers: each thread moves 16-byte vectors, consecutive
+// threads touch consecutive vectors, so every warp reads and writes whole
+// 512-byte runs of a cache row.  The roofline is HBM bandwidth (bytes read +
+// bytes written).
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// One 16-byte vector per thread over the flattened (token, vector) space.
+// A token's K (or V) row, all heads, is contiguous both in the input
+// [T, Hkv, D] and in the cache [P, B, Hkv, D] (flat slot = block * B + offset),
+// so each token is a single contiguous row copy.
+__global__ void __launch_bounds__(kThreads)
+reshape_and_cache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                         uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                         const int64_t *__restrict__ slot_mapping, int num_tokens,
+                         int row_vecs, int64_t num_slots, unsigned int *err) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t t = i / row_vecs;
+    const int e = static_cast<int>(i - t * row_vecs);
+    if (t >= num_tokens) return;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;                         // padding token
+    if (slot >= num_slots) {                      // outside the pool: skip, report
+        if (e == 0) pk::set_error(err, PK_DEVERR_SLOT);
+        return;
+    }
+    const uint4 kv = pk::ldg_stream(k + t * row_vecs + e);
+    const uint4 vv = pk::ldg_stream(v + t * row_vecs + e);
+    k_cache[slot * row_vecs + e] = kv;
+    v_cache[slot * row_vecs + e] = vv;
+}
+
+// grid = (pairs, 2 [K, V], chunks of one block).  Plain loads: the pool is
+// written by this kernel, so the read-only path is not used.
+constexpr int kCopyVecsPerCta = kThreads * 4;
+
+__global__ void __launch_bounds__(kThreads)
+copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                   const int64_t *__restrict__ pairs, int64_t block_vecs, int num_blocks,
+                   unsigned int *err) {
+    const int pair = blockIdx.x;
+    const int64_t src = pairs[2 * pair];
+    const int64_t dst = pairs[2 * pair + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) pk::set_error(err, PK_DEVERR_PAIR);
+        return;
+    }
+    uint4 *c = blockIdx.y ? v_cache : k_cache;
+    const uint4 *s = c + src * block_vecs;
+    uint4 *d = c + dst * block_vecs;
+    const int64_t lo = static_cast<int64_t>(blockIdx.z) * kCopyVecsPerCta;
+    const int64_t hi = min(lo + kCopyVecsPerCta, block_vecs);
+    uint4 buf[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t e = lo + u * kThreads + threadIdx.x;
+        if (e < hi) buf[u] = s[e];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t e = lo + u * kThreads + threadIdx.x;
+        if (e < hi) d[e] = buf[u];
+    }
+}
+
+// grid = (num_seqs, token chunks of kGatherTokens).  Each CTA walks the table
+// of one sequence for its chunk of positions.
+constexpr int kGatherTokens = 32;
+
+__global__ void __launch_bounds__(kThreads)
+gather_kv_kernel(uint4 *__restrict__ out_k, uint4 *__restrict__ out_v,
+                 const uint4 *__restrict__ k_cache, const uint4 *__restrict__ v_cache,
+                 const int32_t *__restrict__ block_tables, int max_blocks_per_seq,
+                 const int32_t *__restrict__ seq_lens, const int64_t *__restrict__ cu_seq_lens,
+                 int max_seq_len, int row_vecs, int num_blocks, int block_size,
+                 unsigned int *err) {
+    const int s = blockIdx.x;
+    int L = seq_lens[s];
+    const int cap = min(max_seq_len, max_blocks_per_seq * block_size);
+    if (L < 0 || L > cap) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) pk::set_error(err, PK_DEVERR_SEQ_LEN);
+        L = L < 0 ? 0 : cap;
+    }
+    const int j0 = blockIdx.y * kGatherTokens;
+    if (j0 >= L) return;
+    const int nj = min(kGatherTokens, L - j0);
+    const int64_t base = cu_seq_lens[s];
+    const int32_t *row = block_tables + static_cast<int64_t>(s) * max_blocks_per_seq;
+    for (int i = threadIdx.x; i < nj * row_vecs; i += kThreads) {
+        const int jj = i / row_vecs;
+        const int e = i - jj * row_vecs;
+        const int j = j0 + jj;
+        const int blk = row[j / block_size];
+        if (blk < 0 || blk >= num_blocks) {
+            if (e == 0) pk::set_error(err, PK_DEVERR_BLOCK_ID);
+            continue;
+        }
+        const int64_t src = (static_cast<int64_t>(blk) * block_size + j % block_size) * row_vecs + e;
+        const int64_t dst = (base + j) * row_vecs + e;
+        out_k[dst] = pk::ldg_stream(k_cache + src);
+        out_v[dst] = pk::ldg_stream(v_cache + src);
+    }
+}
+
+bool supported_geometry(int num_kv_heads, int head_dim, int block_size) {
+    return num_kv_heads >= 1 && (head_dim == 64 || head_dim == 128) &&
+           (block_size == 8 || block_size == 16 || block_size == 32);
+}
+
+}  // namespace
+
+extern "C" int pk_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                                    const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                                    int head_dim, int num_blocks, int block_size,
+                                    pk_stream_t stream) {
+    if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0)
+        return PK_ERR_SHAPE;
+    if (!supported_geometry(num_kv_heads, head_dim, block_size)) return PK_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PK_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PK_ERR_NULL;
+    if (!pk::aligned16(k) || !pk::aligned16(v) || !pk::aligned16(k_cache) || !pk::aligned16(v_cache))
+        return PK_ERR_ALIGNMENT;
+    const int row_vecs = num_kv_heads * head_dim / 8;
+    const int64_t total = static_cast<int64_t>(num_tokens) * row_vecs;
+    const int64_t grid = (total + kThreads - 1) / kThreads;
+    if (grid > 0x7fffffff) return PK_ERR_SHAPE;
+    unsigned int *err = pk::error_word_ptr();
+    if (!err) return PK_ERR_NO_DEVICE;
+    reshape_and_cache_kernel<<<static_cast<unsigned>(grid), kThreads, 0,
+                               reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), slot_mapping, num_tokens, row_vecs,
+        static_cast<int64_t>(num_blocks) * block_size, err);
+    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+extern "C" int pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
+                              int num_pairs, int num_kv_heads, int head_dim, int num_blocks,
+                              int block_size, pk_stream_t stream) {
+    if (num_pairs < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0)
+        return PK_ERR_SHAPE;
+    if (!supported_geometry(num_kv_heads, head_dim, block_size)) return PK_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PK_OK;
+    if (!k_cache || !v_cache || !src_dst_pairs) return PK_ERR_NULL;
+    if (!pk::aligned16(k_cache) || !pk::aligned16(v_cache)) return PK_ERR_ALIGNMENT;
+    const int64_t block_vecs = static_cast<int64_t>(block_size) * num_kv_heads * head_dim / 8;
+    const int64_t chunks = (block_vecs + kCopyVecsPerCta - 1) / kCopyVecsPerCta;
+    if (chunks > 65535) return PK_ERR_SHAPE;
+    unsigned int *err = pk::error_word_ptr();
+    if (!err) return PK_ERR_NO_DEVICE;
+    dim3 grid(static_cast<unsigned>(num_pairs), 2, static_cast<unsigned>(chunks));
+    copy_blocks_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs, block_vecs,
+        num_blocks, err);
+    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+extern "C" int pk_gather_kv(void *out_k, void *out_v, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, const int64_t *cu_seq_lens, int max_seq_len,
+                            int num_seqs, int num_kv_heads, int head_dim, int num_blocks,
+                            int block_size, pk_stream_t stream) {
+    if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_seq_len < 0)
+        return PK_ERR_SHAPE;
+    if (!supported_geometry(num_kv_heads, head_dim, block_size)) return PK_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+        return PK_ERR_SHAPE;
+    if (num_seqs == 0 || max_seq_len == 0) return PK_OK;
+    if (!out_k || !out_v || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_seq_lens)
+        return PK_ERR_NULL;
+    if (!pk::aligned16(out_k) || !pk::aligned16(out_v) || !pk::aligned16(k_cache) ||
+        !pk::aligned16(v_cache))
+        return PK_ERR_ALIGNMENT;
+    const int chunks = (max_seq_len + kGatherTokens - 1) / kGatherTokens;
+    if (chunks > 65535 || num_seqs > 0x7fffffff) return PK_ERR_SHAPE;
+    unsigned int *err = pk::error_word_ptr();
+    if (!err) return PK_ERR_NO_DEVICE;
+    dim3 grid(static_cast<unsigned>(num_seqs), static_cast<unsigned>(chunks));
+    gather_kv_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(out_k), static_cast<uint4 *>(out_v),
+        static_cast<const uint4 *>(k_cache), static_cast<const uint4 *>(v_cache), block_tables,
+        max_blocks_per_seq, seq_lens, cu_seq_lens, max_seq_len, num_kv_heads * head_dim / 8,
+        num_blocks, block_size, err);
+    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}

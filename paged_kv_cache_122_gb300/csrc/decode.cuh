@@ -1,0 +1,45 @@
+// Parameters and launchers of the paged decode-attention kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace pk {
+
+// Everything a decode kernel needs, by value.  Scores are kept in the base-2
+// domain: s2 = (q . k) * scale * log2(e), weights are 2^(s2 - m).
+struct DecodeParams {
+    void *out;
+    int out_fp32;
+    const uint16_t *q;          // [N, H, D]
+    const uint16_t *k_cache;    // [P, B, Hkv, D]
+    const uint16_t *v_cache;
+    const int32_t *block_tables;  // [N, MB]
+    const int32_t *seq_lens;      // [N]
+    int max_blocks_per_seq;
+    int max_seq_len;
+    int num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size;
+    float scale_log2;
+    // Split-K partials, indexed by u = (s * H + h) * np_cap + partition:
+    // ws_m[u] running max (base 2), ws_l[u] denominator, ws_o[u * D + d]
+    // unnormalised output.
+    float *ws_m;
+    float *ws_l;
+    float *ws_o;
+    int part_tokens;   // tokens per partition (multiple of 128)
+    int np_cap;        // partitions reserved per (sequence, head)
+    unsigned int *err;
+};
+
+// Smallest partition any decode path uses; fixes the workspace bound.
+constexpr int kMinPartTokens = 256;
+
+inline size_t workspace_floats(int num_seqs, int num_heads, int head_dim, int np_cap) {
+    return static_cast<size_t>(num_seqs) * num_heads * np_cap * (head_dim + 2);
+}
+
+// CUDA-core path (any supported G).  Returns a cudaError_t.
+cudaError_t launch_decode_cuda_core(const DecodeParams &p, cudaStream_t stream);
+// Log-sum-exp merge of the partitions of split sequences.
+cudaError_t launch_decode_merge(const DecodeParams &p, cudaStream_t stream);
+
+}  // namespace pk

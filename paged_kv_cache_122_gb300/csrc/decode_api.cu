@@ -1,0 +1,92 @@
+// Host entry point of paged decode attention: argument checks, the split-K
+// plan and the launches.
+#include "decode.cuh"
+
+#include <algorithm>
+#include <cmath>
+
+namespace {
+
+bool group_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
+// Partition size of the CUDA-core path.
+constexpr int kCudaCorePartTokens = 512;
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace
+
+extern "C" size_t pk_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                            int head_dim, int max_seq_len) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0) return 0;
+    if (num_heads % num_kv_heads) return 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
+    const int np_cap = ceil_div(max_seq_len, pk::kMinPartTokens);
+    if (np_cap <= 1) return 0;
+    return pk::workspace_floats(num_seqs, num_heads, head_dim, np_cap) * sizeof(float);
+}
+
+extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q,
+                                         const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, int max_blocks_per_seq,
+                                         const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                                         int num_heads, int num_kv_heads, int head_dim,
+                                         int num_blocks, int block_size, float scale,
+                                         void *workspace, size_t workspace_bytes,
+                                         pk_stream_t stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
+        max_blocks_per_seq < 0 || max_seq_len < 0 || block_size <= 0)
+        return PK_ERR_SHAPE;
+    if (num_heads % num_kv_heads) return PK_ERR_SHAPE;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+        return PK_ERR_SHAPE;
+    if (out_dtype != PK_BF16 && out_dtype != PK_FP32) return PK_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PK_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PK_ERR_UNSUPPORTED;
+    if (!group_supported(num_heads / num_kv_heads)) return PK_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PK_ERR_SHAPE;
+    if (num_seqs > 65535 || num_kv_heads * 2 > 65535) return PK_ERR_SHAPE;
+    if (num_seqs == 0) return PK_OK;
+    if (!out || !q || !seq_lens || (max_seq_len > 0 && (!k_cache || !v_cache || !block_tables)))
+        return PK_ERR_NULL;
+    if (!pk::aligned16(out) || !pk::aligned16(q) || !pk::aligned16(k_cache) || !pk::aligned16(v_cache))
+        return PK_ERR_ALIGNMENT;
+
+    pk::DecodeParams p{};
+    p.out = out;
+    p.out_fp32 = out_dtype == PK_FP32;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k_cache = static_cast<const uint16_t *>(k_cache);
+    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_seq_len = max_seq_len;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.scale_log2 = scale * pk::kLog2e;
+    p.part_tokens = kCudaCorePartTokens;
+    p.np_cap = std::max(1, ceil_div(max_seq_len, p.part_tokens));
+
+    if (p.np_cap > 1) {
+        const size_t need = pk::workspace_floats(num_seqs, num_heads, head_dim, p.np_cap) * sizeof(float);
+        if (!workspace || workspace_bytes < need) return PK_ERR_WORKSPACE;
+        if (!pk::aligned16(workspace)) return PK_ERR_ALIGNMENT;
+        float *ws = static_cast<float *>(workspace);
+        const size_t rows = static_cast<size_t>(num_seqs) * num_heads * p.np_cap;
+        p.ws_o = ws;
+        p.ws_m = ws + rows * head_dim;
+        p.ws_l = p.ws_m + rows;
+    }
+
+    p.err = pk::error_word_ptr();
+    if (!p.err) return PK_ERR_NO_DEVICE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (pk::launch_decode_cuda_core(p, st) != cudaSuccess) return PK_ERR_CUDA;
+    if (pk::launch_decode_merge(p, st) != cudaSuccess) return PK_ERR_CUDA;
+    return PK_OK;
+}
