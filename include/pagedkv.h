@@ -74,6 +74,8 @@ enum pk_dtype { PK_BF16 = 0, PK_FP32 = 1 };
 #define PK_DEVERR_PAIR     0x4u /* a copy pair names a block outside [0, num_blocks) */
 #define PK_DEVERR_SEQ_LEN  0x8u /* a seq_len is negative, exceeds max_seq_len or exceeds
                                    max_blocks_per_seq * block_size */
+#define PK_DEVERR_TIMEOUT  0x10u /* a kernel gave up waiting on one of its own pipeline
+                                    barriers (never expected; the results are invalid) */
 
 /* Human-readable name of a pk_status value; never NULL. */
 const char *pk_status_string(int status);
@@ -138,6 +140,22 @@ int pk_paged_attention_decode(void *out, int out_dtype, const void *q,
                               int head_dim, int num_blocks, int block_size,
                               float scale, void *workspace, size_t workspace_bytes,
                               pk_stream_t stream);
+
+/* Kernel family of pk_paged_attention_decode, process-wide. */
+enum pk_decode_path {
+    PK_PATH_AUTO = 0,         /* tensor cores when G >= 4, CUDA cores otherwise */
+    PK_PATH_CUDA_CORE = 1,    /* fp32 FMA on CUDA cores, one CTA per partition */
+    PK_PATH_TENSOR_CORE = 2   /* tcgen05 MMA with TMEM accumulators, persistent CTAs */
+};
+
+/*
+ * Select the decode kernel family for later calls (all devices); returns the
+ * previous setting, or PK_ERR_UNSUPPORTED for an unknown value.  Both
+ * families compute the same attention; they differ in how the score and
+ * output contractions are executed.  Not synchronised with calls in flight on
+ * other host threads.
+ */
+int pk_set_decode_path(int path);
 
 /*
  * Append new tokens' K/V to their cache slots ("vLLM — PagedAttention",

@@ -19,6 +19,7 @@ from .api import (  # noqa: F401
     pk_get_device_error,
     pk_paged_attention_decode,
     pk_reshape_and_cache,
+    pk_set_decode_path,
     reshape_and_cache,
 )
 from ._native import PagedKVError, load as load_library  # noqa: F401

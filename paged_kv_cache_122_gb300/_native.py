@@ -35,6 +35,7 @@ SIGNATURES = {
         c_void_p, c_int, c_void_p, c_void_p, c_int,
         c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "pk_get_device_error": (c_int, [ctypes.POINTER(c_uint), c_void_p]),
+    "pk_set_decode_path": (c_int, [c_int]),
 }
 
 PK_OK = 0
@@ -43,7 +44,8 @@ STATUS_NAMES = {
     0: "PK_OK", -1: "PK_ERR_NULL", -2: "PK_ERR_SHAPE", -3: "PK_ERR_UNSUPPORTED",
     -4: "PK_ERR_WORKSPACE", -5: "PK_ERR_CUDA", -6: "PK_ERR_ALIGNMENT", -7: "PK_ERR_NO_DEVICE",
 }
-DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_SEQ_LEN = 0x1, 0x2, 0x4, 0x8
+DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
 
 _lib = None
 

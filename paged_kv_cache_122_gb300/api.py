@@ -188,6 +188,20 @@ def pk_gather_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: tor
     return out_k[:total], out_v[:total], cu_t
 
 
+def pk_set_decode_path(path) -> int:
+    """Choose the decode kernel family: "auto", "cuda_core" or "tensor_core" (or 0/1/2).
+
+    Returns the previous setting as an int.
+    """
+    names = {"auto": _native.PATH_AUTO, "cuda_core": _native.PATH_CUDA_CORE,
+             "tensor_core": _native.PATH_TENSOR_CORE}
+    code = names[path] if isinstance(path, str) else int(path)
+    prev = load().pk_set_decode_path(code)
+    if prev < 0:
+        check("pk_set_decode_path", prev)
+    return prev
+
+
 def pk_get_device_error(device=None, stream=None) -> int:
     """Read and clear the device error word (synchronises the stream)."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())

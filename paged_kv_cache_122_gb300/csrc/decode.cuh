@@ -27,6 +27,8 @@ struct DecodeParams {
     float *ws_o;
     int part_tokens;   // tokens per partition (multiple of 128)
     int np_cap;        // partitions reserved per (sequence, head)
+    // Tensor-core path: two cut-segment slots per CTA.
+    void *tc_slots;
     unsigned int *err;
 };
 
@@ -36,6 +38,11 @@ constexpr int kMinPartTokens = 256;
 inline size_t workspace_floats(int num_seqs, int num_heads, int head_dim, int np_cap) {
     return static_cast<size_t>(num_seqs) * num_heads * np_cap * (head_dim + 2);
 }
+
+// Tensor-core path (tcgen05): main kernel + merge of cut segments.
+cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream);
+// Workspace bytes the tensor-core path needs (independent of the sizes).
+size_t tc_workspace_bytes();
 
 // CUDA-core path (any supported G).  Returns a cudaError_t.
 cudaError_t launch_decode_cuda_core(const DecodeParams &p, cudaStream_t stream);

@@ -3,6 +3,7 @@
 #include "decode.cuh"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 namespace {
@@ -11,6 +12,13 @@ bool group_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G =
 
 // Partition size of the CUDA-core path.
 constexpr int kCudaCorePartTokens = 512;
+
+// Smallest group for which the automatic choice uses the tensor cores: from
+// G = 4 on, the scores of a 128-token tile are a [128 x D] x [D x G]
+// contraction and fp32 FMA issue, not HBM, would bound the CUDA-core kernel.
+constexpr int kTensorCoreMinGroup = 4;
+
+std::atomic<int> g_path{PK_PATH_AUTO};
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -22,8 +30,15 @@ extern "C" size_t pk_decode_workspace_bytes(int num_seqs, int num_heads, int num
     if (num_heads % num_kv_heads) return 0;
     if (head_dim != 64 && head_dim != 128) return 0;
     const int np_cap = ceil_div(max_seq_len, pk::kMinPartTokens);
-    if (np_cap <= 1) return 0;
-    return pk::workspace_floats(num_seqs, num_heads, head_dim, np_cap) * sizeof(float);
+    // Enough for either kernel family (the family can be switched at run time).
+    const size_t cc = np_cap > 1 ? pk::workspace_floats(num_seqs, num_heads, head_dim, np_cap) * sizeof(float) : 0;
+    const size_t tc = max_seq_len > 128 ? pk::tc_workspace_bytes() : 0;
+    return std::max(cc, tc);
+}
+
+extern "C" int pk_set_decode_path(int path) {
+    if (path != PK_PATH_AUTO && path != PK_PATH_CUDA_CORE && path != PK_PATH_TENSOR_CORE) return PK_ERR_UNSUPPORTED;
+    return g_path.exchange(path);
 }
 
 extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q,
@@ -69,23 +84,35 @@ extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q
     p.num_blocks = num_blocks;
     p.block_size = block_size;
     p.scale_log2 = scale * pk::kLog2e;
-    p.part_tokens = kCudaCorePartTokens;
-    p.np_cap = std::max(1, ceil_div(max_seq_len, p.part_tokens));
-
-    if (p.np_cap > 1) {
-        const size_t need = pk::workspace_floats(num_seqs, num_heads, head_dim, p.np_cap) * sizeof(float);
-        if (!workspace || workspace_bytes < need) return PK_ERR_WORKSPACE;
-        if (!pk::aligned16(workspace)) return PK_ERR_ALIGNMENT;
-        float *ws = static_cast<float *>(workspace);
-        const size_t rows = static_cast<size_t>(num_seqs) * num_heads * p.np_cap;
-        p.ws_o = ws;
-        p.ws_m = ws + rows * head_dim;
-        p.ws_l = p.ws_m + rows;
+    const int path = g_path.load();
+    const int G = num_heads / num_kv_heads;
+    const bool tensor_core = max_seq_len > 0 &&
+        (path == PK_PATH_TENSOR_CORE || (path == PK_PATH_AUTO && G >= kTensorCoreMinGroup));
+    if (tensor_core) {
+        if (max_seq_len > 128) {          // a sequence may span several CTAs: partials need slots
+            if (!workspace || workspace_bytes < pk::tc_workspace_bytes()) return PK_ERR_WORKSPACE;
+            if (!pk::aligned16(workspace)) return PK_ERR_ALIGNMENT;
+            p.tc_slots = workspace;
+        }
+    } else {
+        p.part_tokens = kCudaCorePartTokens;
+        p.np_cap = std::max(1, ceil_div(max_seq_len, p.part_tokens));
+        if (p.np_cap > 1) {
+            const size_t need = pk::workspace_floats(num_seqs, num_heads, head_dim, p.np_cap) * sizeof(float);
+            if (!workspace || workspace_bytes < need) return PK_ERR_WORKSPACE;
+            if (!pk::aligned16(workspace)) return PK_ERR_ALIGNMENT;
+            float *ws = static_cast<float *>(workspace);
+            const size_t rows = static_cast<size_t>(num_seqs) * num_heads * p.np_cap;
+            p.ws_o = ws;
+            p.ws_m = ws + rows * head_dim;
+            p.ws_l = p.ws_m + rows;
+        }
     }
 
     p.err = pk::error_word_ptr();
     if (!p.err) return PK_ERR_NO_DEVICE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (tensor_core) return pk::launch_decode_tensor_core(p, st) == cudaSuccess ? PK_OK : PK_ERR_CUDA;
     if (pk::launch_decode_cuda_core(p, st) != cudaSuccess) return PK_ERR_CUDA;
     if (pk::launch_decode_merge(p, st) != cudaSuccess) return PK_ERR_CUDA;
     return PK_OK;

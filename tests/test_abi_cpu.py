@@ -47,12 +47,16 @@ def test_status_strings_and_version(lib):
     for code in _native.STATUS_NAMES:
         assert lib.pk_status_string(code)
     assert lib.pk_status_string(12345) == b"unknown status"
+    assert lib.pk_set_decode_path(7) == -3
+    assert lib.pk_set_decode_path(1) == 0 and lib.pk_set_decode_path(0) == 1
 
 
 def test_workspace_bound(lib):
     f = lib.pk_decode_workspace_bytes
-    assert f(4, 8, 8, 64, 129) == 0                     # one partition: no workspace
-    assert f(8, 32, 8, 128, 131072) == 8 * 32 * 512 * 130 * 4
+    slots = 2 * 1024 * 8384                             # tensor-core path: two cut-segment slots per CTA
+    assert f(4, 8, 8, 64, 128) == 0                     # one tile per sequence: nothing is ever split
+    assert f(4, 8, 8, 64, 129) == slots
+    assert f(8, 32, 8, 128, 131072) == max(8 * 32 * 512 * 130 * 4, slots)
     assert f(1, 6, 4, 128, 4096) == 0                   # 6 % 4 != 0
     assert f(1, 8, 8, 96, 4096) == 0                    # head_dim unsupported
     assert f(-1, 8, 8, 64, 10) == 0

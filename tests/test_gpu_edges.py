@@ -13,6 +13,14 @@ from paritylib import assert_close, host_bits
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
+PATHS = ["cuda_core", "tensor_core"]
+
+
+@pytest.fixture
+def decode_path(request):
+    prev = pk.pk_set_decode_path(request.param)
+    yield request.param
+    pk.pk_set_decode_path(prev)
 
 EDGE_LENS = [0, 1, 2, 7, 8, 15, 16, 17, 31, 32, 33, 255, 256, 257, 511, 512, 513, 1023, 1024, 1025, 2047, 4103]
 
@@ -28,9 +36,10 @@ def _ref(w, t):
                                          w.block_tables, w.seq_lens, w.scale, w.block_size)
 
 
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
 @pytest.mark.parametrize("pad", ["neg1", "garbage"])
 @pytest.mark.parametrize("B", [8, 16, 32])
-def test_boundary_lengths(B, pad):
+def test_boundary_lengths(B, pad, decode_path):
     w = W.custom(3, EDGE_LENS, 32, 8, 128, B, pad=pad)
     t = W.make_tensors(w, DEV)
     for dt in (torch.float32, torch.bfloat16):
@@ -41,9 +50,10 @@ def test_boundary_lengths(B, pad):
     assert pk.pk_get_device_error() == 0
 
 
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
-def test_group_and_head_dim(G, D):
+def test_group_and_head_dim(G, D, decode_path):
     Hkv = 2
     w = W.custom(4, [1, 40, 700, 1500], G * Hkv, Hkv, D, 16)
     t = W.make_tensors(w, DEV)
@@ -51,7 +61,8 @@ def test_group_and_head_dim(G, D):
     assert_close(out.cpu().numpy(), _ref(w, t), False, f"G={G} D={D}")
 
 
-def test_physical_relabelling_gives_identical_bits():
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
+def test_physical_relabelling_gives_identical_bits(decode_path):
     w = W.custom(5, [3, 300, 1000, 2500], 32, 8, 128, 16)
     t = W.make_tensors(w, DEV)
     base = _attend(w, t, torch.bfloat16).clone()
@@ -91,7 +102,8 @@ def test_block_size_invariance():
     assert np.abs(outs[2] - outs[1]).max() < 2e-5
 
 
-def test_deterministic_and_guard_bytes_untouched():
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
+def test_deterministic_and_guard_bytes_untouched(decode_path):
     w = W.get("l3-8b", 0)
     t = W.make_tensors(w, DEV)
     N, H, D = w.num_seqs, w.num_heads, w.head_dim
@@ -113,7 +125,8 @@ def test_non_default_stream():
     assert_close(out.cpu().numpy(), _ref(w, t), False, "stream")
 
 
-def test_bad_block_id_is_reported_not_faulted():
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
+def test_bad_block_id_is_reported_not_faulted(decode_path):
     w = W.custom(7, [40, 40], 8, 2, 64, 16)
     t = W.make_tensors(w, DEV)
     pk.pk_get_device_error()
