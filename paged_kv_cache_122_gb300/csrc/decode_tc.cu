@@ -545,10 +545,13 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
     const int64_t start = mine->start_tile, T = mine->total_tiles;
     int ca = static_cast<int>(start * C / T);
     while (ca + 1 < C && range_begin(ca + 1, T, C) <= start) ++ca;
+    // Contributors are the CTAs from ca to c with a non-empty range (when the
+    // grid has more CTAs than tiles, some ranges are empty and hold no slot).
     float M[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) M[g] = -INFINITY;
     for (int cc = ca; cc <= c; ++cc) {
+        if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
         const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
 #pragma unroll
         for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], sl->m[g]);
@@ -559,6 +562,7 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
 #pragma unroll
     for (int g = 0; g < G; ++g) num[g] = den[g] = 0.f;
     for (int cc = ca; cc <= c; ++cc) {
+        if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
         const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
