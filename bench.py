@@ -191,6 +191,18 @@ def dist_setup():
     return ws, rank, local
 
 
+def aggregate_over_ranks(device_ms: float, e2e_ms: float, step_bytes: float, device):
+    """Whole-job figures over the ranks: the slowest rank's times and the sum
+    of every rank's bytes (each rank runs its own batch)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([device_ms, e2e_ms], dtype=torch.float64, device=device)
+    b = torch.tensor([step_bytes], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t[0]), float(t[1]), float(b[0])
+
+
 def run_ours(args):
     import torch
     import paged_kv_cache_122_gb300 as pk
@@ -200,6 +212,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk.load_library()
+    pk.pk_set_decode_path(args.decode_path)
     w = W.get(args.workload, args.seed + rank)
     t = W.make_tensors(w, dev)
     ub = M.useful_bytes(w)
@@ -219,8 +232,12 @@ def run_ours(args):
         if w.num_new_tokens:
             pk.reshape_and_cache(kn, vn, t["k_cache"], t["v_cache"], sm)
 
-    launches_per_step = (1 if w.copy_pairs.shape[0] else 0) + (1 if w.num_new_tokens else 0) + 1 + \
-        (1 if w.max_seq_len > 512 else 0)
+    # Launches of this library per step: copy, append, then the decode kernel
+    # and its merge (the merge runs when a sequence can span several CTAs /
+    # partitions: > 128 tokens on tensor cores, > 512 on CUDA cores).
+    tensor_core = args.decode_path == "tensor_core" or (args.decode_path == "auto" and w.group >= 4)
+    merge = w.max_seq_len > (128 if tensor_core else 512)
+    launches_per_step = (1 if w.copy_pairs.shape[0] else 0) + (1 if w.num_new_tokens else 0) + 1 + (1 if merge else 0)
 
     for _ in range(args.warmup):
         prelude()
@@ -274,13 +291,7 @@ def run_ours(args):
     assert pk.pk_get_device_error(dev) == 0
 
     if ws > 1:
-        import torch.distributed as dist
-        vals = torch.tensor([total_ms, e2e_ms, float(ub["step"])], dtype=torch.float64, device=dev)
-        mx = vals.clone()
-        dist.all_reduce(mx[:2], op=dist.ReduceOp.MAX)
-        sm = vals.clone()
-        dist.all_reduce(sm[2:], op=dist.ReduceOp.SUM)
-        total_ms, e2e_ms, all_bytes = float(mx[0]), float(mx[1]), float(sm[2])
+        total_ms, e2e_ms, all_bytes = aggregate_over_ranks(total_ms, e2e_ms, float(ub["step"]), dev)
     else:
         all_bytes = float(ub["step"])
 
@@ -317,6 +328,7 @@ def run_ours(args):
             "unique_kv_bytes": ub["kv_unique"],
             "l2": "flushed between timed steps (256 MiB write outside the events); K/V inputs also exceed L2",
             "parallelism": f"replicas x{ws} (independent batches, no collective)",
+            "decode_path": args.decode_path,
         },
         "pct_of_peak": round(100.0 * value / peak, 2),
         "tokens_per_s_per_layer": round(w.num_seqs * ws / (ms_per_step * 1e-3), 1),
@@ -404,6 +416,8 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-seqs", type=int, default=32)
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core"],
+                    help="kernel family of paged_attention_decode (auto: tensor cores for G >= 4)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
