@@ -141,6 +141,43 @@ int pk_paged_attention_decode(void *out, int out_dtype, const void *q,
                               float scale, void *workspace, size_t workspace_bytes,
                               pk_stream_t stream);
 
+/*
+ * The same decode attention as pk_paged_attention_decode, for callers that
+ * cannot allocate device memory.  The pages have no counterpart of this call.
+ *
+ * Who needs it: code running inside a host program that owns all device
+ * memory (a serving engine that reserved nearly all HBM for its KV pool at
+ * start-up, so a later cudaMalloc fails), plugins that are handed tensors but
+ * no allocator, and latency-critical loops that cannot afford cudaMalloc /
+ * cudaFree, which may synchronise the device.  Such callers pass only the
+ * inputs and the output; this call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *
+ * Scratch: the partial results of sequences that span several CTAs go to a
+ * fixed 2,682,880-byte array in the library's own device memory (a file-scope
+ * __device__ array that every GPU loading the library holds until the
+ * process exits): two 8,384-byte slots for each of at most 160 persistent
+ * CTAs.  The call runs min(SM count, 160) CTAs; if that many slots did not
+ * fit the array it would return PK_ERR_WORKSPACE.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * Sharing: every call on a device uses the same array and leaves its contents
+ * there.  Nothing in it has to start at zero (each CTA writes its own flag
+ * before use), but calls that overlap on the GPU (several streams, or host
+ * threads without ordering) race on it and give wrong results: order them.
+ *
+ * Arguments, layouts and errors are those of pk_paged_attention_decode
+ * without the workspace.  The tensor-core kernel family is always used.
+ */
+int pk_paged_attention_decode_noalloc(void *out, int out_dtype, const void *q,
+                                      const void *k_cache, const void *v_cache,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *seq_lens, int max_seq_len,
+                                      int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_dim, int num_blocks, int block_size,
+                                      float scale, pk_stream_t stream);
+
 /* Kernel family of pk_paged_attention_decode, process-wide. */
 enum pk_decode_path {
     PK_PATH_AUTO = 0,         /* tensor cores when G >= 4, CUDA cores otherwise */

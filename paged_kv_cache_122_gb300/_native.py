@@ -25,6 +25,9 @@ SIGNATURES = {
         c_int, c_int, c_int, c_int,            # num_seqs, num_heads, num_kv_heads, head_dim
         c_int, c_int, c_float,                 # num_blocks, block_size, scale
         c_void_p, c_size_t, c_void_p]),        # workspace, workspace_bytes, stream
+    "pk_paged_attention_decode_noalloc": (c_int, [
+        c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
+        c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p]),
     "pk_reshape_and_cache": (c_int, [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
         c_int, c_int, c_int, c_int, c_int, c_void_p]),

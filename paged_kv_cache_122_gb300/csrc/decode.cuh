@@ -43,6 +43,11 @@ inline size_t workspace_floats(int num_seqs, int num_heads, int head_dim, int np
 cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream);
 // Workspace bytes the tensor-core path needs (independent of the sizes).
 size_t tc_workspace_bytes();
+// Bytes of one cut-segment slot of the tensor-core path (two per CTA).
+size_t tc_slot_bytes();
+// Tensor-core path with an explicit grid of `ctas` persistent CTAs; the
+// slots at p.tc_slots must hold 2 * ctas slots.
+cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas);
 
 // CUDA-core path (any supported G).  Returns a cudaError_t.
 cudaError_t launch_decode_cuda_core(const DecodeParams &p, cudaStream_t stream);

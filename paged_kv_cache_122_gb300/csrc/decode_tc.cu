@@ -667,3 +667,17 @@ cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream
 }
 
 }  // namespace pk
+
+namespace pk {
+
+size_t tc_slot_bytes() { return sizeof(Slot); }
+
+cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas) {
+    CUtensorMap mk, mv, mq;
+    if (ctas <= 0 || ctas > static_cast<int>(kMaxCtas)) return cudaErrorInvalidValue;
+    if (!encode_cache_map(&mk, p.k_cache, p) || !encode_cache_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
+        return cudaErrorInvalidValue;
+    return p.head_dim == 64 ? launch_d<64>(mk, mv, mq, p, ctas, stream) : launch_d<128>(mk, mv, mq, p, ctas, stream);
+}
+
+}  // namespace pk
