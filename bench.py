@@ -203,6 +203,66 @@ def aggregate_over_ranks(device_ms: float, e2e_ms: float, step_bytes: float, dev
     return float(t[0]), float(t[1]), float(b[0])
 
 
+def contiguous_tables(w):
+    """Block tables of the same lengths with every sequence's blocks back to
+    back (bt[s, i] = base_s + i): the paging-overhead control layout."""
+    import numpy as np
+    bt = np.full_like(w.block_tables, -1)
+    base = 0
+    for s in range(w.num_seqs):
+        nb = -(-int(w.seq_lens[s]) // w.block_size)
+        bt[s, :nb] = np.arange(base, base + nb, dtype=np.int32)
+        base += nb
+    assert base <= w.num_blocks
+    return bt
+
+
+def time_decode(fn, steps, flush, stream):
+    """Mean device time (ms) of fn() over `steps` calls, L2 flushed before each."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def workload_report(name, seed, dev, steps, flush, peak):
+    """Decode-only GB/s of another workload (context for the bench line)."""
+    import torch
+    import paged_kv_cache_122_gb300 as pk
+    from paged_kv_cache_122_gb300 import metrics as M, workloads as W
+    w = W.get(name, seed)
+    t = W.make_tensors(w, dev)
+    ub = M.useful_bytes(w)
+    ws = torch.empty(max(1, pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                        w.max_seq_len)), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    if w.copy_pairs.shape[0]:
+        pk.copy_blocks(t["k_cache"], t["v_cache"], t["copy_pairs"])
+    if w.num_new_tokens:
+        pk.reshape_and_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+
+    def fn():
+        pk.pk_paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"],
+                                     w.scale, w.block_size, w.max_seq_len, ws)
+    for _ in range(3):
+        fn()
+    ms = time_decode(fn, steps, flush, torch.cuda.current_stream(dev))
+    gbs = ub["attention"] / (ms * 1e-3) / 1e9
+    rep = {"decode_ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+           "tokens_per_s_per_layer": round(w.num_seqs / (ms * 1e-3), 1)}
+    if ub["kv_unique"] != ub["kv"]:
+        uniq = (ub["attention"] - ub["kv"] + ub["kv_unique"]) / (ms * 1e-3) / 1e9
+        rep["gbs_unique_bytes"] = round(uniq, 1)
+    del t, ws, out
+    torch.cuda.empty_cache()
+    return rep
+
+
 def run_ours(args):
     import torch
     import paged_kv_cache_122_gb300 as pk
@@ -235,8 +295,10 @@ def run_ours(args):
     # Launches of this library per step: copy, append, then the decode kernel
     # and its merge (the merge runs when a sequence can span several CTAs /
     # partitions: > 128 tokens on tensor cores, > 512 on CUDA cores).
-    tensor_core = args.decode_path == "tensor_core" or (args.decode_path == "auto" and w.group >= 4)
-    merge = w.max_seq_len > (128 if tensor_core else 512)
+    tensor_core = args.decode_path.startswith("tensor_core") or (args.decode_path == "auto" and w.group >= 4)
+    head_batched = args.decode_path == "tensor_core_head_batched" and w.num_kv_heads == 8 and \
+        w.block_size in (16, 32) and w.group <= 8
+    merge = (not head_batched) and w.max_seq_len > (128 if tensor_core else 512)   # fused when head-batched
     launches_per_step = (1 if w.copy_pairs.shape[0] else 0) + (1 if w.num_new_tokens else 0) + 1 + (1 if merge else 0)
 
     for _ in range(args.warmup):
@@ -289,6 +351,20 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
     assert pk.pk_get_device_error(dev) == 0
+
+    # Paging-overhead control: the same kernel and lengths, contiguous tables.
+    bt_contig = torch.from_numpy(contiguous_tables(w)).to(dev)
+    ctl_steps = max(10, min(args.steps, 100))
+    paged_ms = time_decode(lambda: attend(), ctl_steps, flush, stream)
+    contig_ms = time_decode(lambda: attend(bt=bt_contig), ctl_steps, flush, stream)
+    assert pk.pk_get_device_error(dev) == 0
+
+    others = {}
+    if args.report_workloads and rank == 0:
+        peak0, _ = load_peaks()
+        for name in ("l3-8b", "long", "prefix-b8", "prefix-b16", "prefix-b32", "tiny"):
+            if name != args.workload:
+                others[name] = workload_report(name, args.seed, dev, 20, flush, peak0)
 
     if ws > 1:
         total_ms, e2e_ms, all_bytes = aggregate_over_ranks(total_ms, e2e_ms, float(ub["step"]), dev)
@@ -351,9 +427,18 @@ def run_ours(args):
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms / args.steps, 5),
         },
+        "paging_overhead": {
+            "paged_decode_ms": round(paged_ms, 5),
+            "contiguous_decode_ms": round(contig_ms, 5),
+            "overhead": round(paged_ms / contig_ms - 1.0, 4),
+            "note": "same kernel and lengths with bt[s, i] = base_s + i; the pages quote a 20-26% kernel "
+                    "slowdown vs a contiguous kernel for the 2023 paged kernel (context, not a target)",
+        },
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if others:
+        res["other_workloads"] = others
     if not args.no_cpu_baseline:
         r = run_cpu_oracle(args.workload, args.seed, args.cpu_seqs, args.cpu_budget)
         tot = sum(r["times"])
@@ -413,10 +498,12 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--report-workloads", action="store_true",
+                    help="also time decode alone on the other workloads (extra context in the line)")
     ap.add_argument("--cpu-seqs", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-seqs", type=int, default=32)
-    ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core"],
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core", "tensor_core_head_batched"],
                     help="kernel family of paged_attention_decode (auto: tensor cores for G >= 4)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps

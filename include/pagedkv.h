@@ -180,9 +180,16 @@ int pk_paged_attention_decode_noalloc(void *out, int out_dtype, const void *q,
 
 /* Kernel family of pk_paged_attention_decode, process-wide. */
 enum pk_decode_path {
-    PK_PATH_AUTO = 0,         /* tensor cores when G >= 4, CUDA cores otherwise */
-    PK_PATH_CUDA_CORE = 1,    /* fp32 FMA on CUDA cores, one CTA per partition */
-    PK_PATH_TENSOR_CORE = 2   /* tcgen05 MMA with TMEM accumulators, persistent CTAs */
+    PK_PATH_AUTO = 0,                    /* tensor cores (per-head tiles) when G >= 4,
+                                            CUDA cores otherwise */
+    PK_PATH_CUDA_CORE = 1,               /* fp32 FMA on CUDA cores, one CTA per partition */
+    PK_PATH_TENSOR_CORE = 2,             /* tcgen05 MMA, persistent CTAs, tiles of
+                                            128 tokens x 1 KV head */
+    PK_PATH_TENSOR_CORE_HEAD_BATCHED = 3 /* tcgen05 MMA, persistent CTAs, tiles of
+                                            16 tokens x all KV heads, merge fused into the
+                                            kernel; used where it applies (num_kv_heads == 8,
+                                            block_size 16 or 32, G <= 8), per-head tiles
+                                            otherwise */
 };
 
 /*

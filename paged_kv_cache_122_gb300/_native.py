@@ -48,7 +48,7 @@ STATUS_NAMES = {
     -4: "PK_ERR_WORKSPACE", -5: "PK_ERR_CUDA", -6: "PK_ERR_ALIGNMENT", -7: "PK_ERR_NO_DEVICE",
 }
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_TENSOR_CORE_HEAD_BATCHED = 0, 1, 2, 3
 
 _lib = None
 

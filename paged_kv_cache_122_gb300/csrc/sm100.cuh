@@ -73,6 +73,11 @@ SM100_DEV void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
+// Bring `bytes` (a multiple of 16, 16-byte aligned source) into L2.
+SM100_DEV void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
 SM100_DEV void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -135,6 +140,65 @@ SM100_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// N consecutive 32-bit columns (N in {2, 4, 8, 16, 32}) of this thread's
+// TMEM lane, 32x32b shape; waits for the load to land.
+template <int N>
+SM100_DEV void tmem_ld(uint32_t taddr, float (&v)[N]) {
+    static_assert(N == 2 || N == 4 || N == 8 || N == 16 || N == 32, "tmem_ld width");
+    if constexpr (N == 16) {
+        tmem_ld16(taddr, v);
+    } else if constexpr (N == 32) {
+        float a[16], b[16];
+        tmem_ld16(taddr, a);
+        tmem_ld16(taddr + 16, b);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { v[i] = a[i]; v[16 + i] = b[i]; }
+    } else {
+        uint32_t r[N];
+        __syncwarp();
+        if constexpr (N == 2) {
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
+                         : "=r"(r[0]), "=r"(r[1]) : "r"(taddr) : "memory");
+        } else if constexpr (N == 4) {
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr) : "memory");
+        } else {
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                           "=r"(r[7])
+                         : "r"(taddr)
+                         : "memory");
+        }
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
+    }
+}
+
+// Store 8 consecutive 32-bit columns of this thread's TMEM lane (32x32b) and
+// wait for the store to complete.
+SM100_DEV void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    __syncwarp();
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                   "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                   "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Named barrier over `nthreads` threads that also ORs a predicate across them.
+SM100_DEV bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(out) : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads) : "memory");
+    return out != 0;
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), version 1, layout type in bits 61-63
 // (0 = no swizzle, 2 = 128-byte swizzle).
@@ -152,7 +216,7 @@ constexpr uint32_t kLayoutSw128 = 2;
 
 // Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B,
 // A / B major-ness (0 = K-major, 1 = MN-major), N and M.
-constexpr uint32_t idesc_bf16(uint32_t m, uint32_t n, uint32_t a_mn_major, uint32_t b_mn_major) {
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t m, uint32_t n, uint32_t a_mn_major, uint32_t b_mn_major) {
     return (1u << 4)                // D format: f32
          | (1u << 7)                // A format: bf16
          | (1u << 10)               // B format: bf16

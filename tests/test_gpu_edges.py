@@ -13,7 +13,7 @@ from paritylib import assert_close, host_bits
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-PATHS = ["cuda_core", "tensor_core"]
+PATHS = ["cuda_core", "tensor_core", "tensor_core_head_batched"]
 
 
 @pytest.fixture
@@ -98,8 +98,12 @@ def test_block_size_invariance():
         t["k_cache"] = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16).to(DEV)
         t["v_cache"] = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16).to(DEV)
         outs.append(_attend(w, t).cpu().numpy())
-    assert np.abs(outs[0] - outs[1]).max() < 2e-5
-    assert np.abs(outs[2] - outs[1]).max() < 2e-5
+        if B == 16:
+            ref = _ref(w, t)
+    # Same logical K/V, three block sizes (and, on tensor cores, different
+    # kernels): every result is within the parity bound of the same oracle.
+    for B, o in zip(ws, outs):
+        assert_close(o, ref, False, f"block size {B}")
 
 
 @pytest.mark.parametrize("decode_path", PATHS, indirect=True)
@@ -126,8 +130,9 @@ def test_non_default_stream():
 
 
 @pytest.mark.parametrize("decode_path", PATHS, indirect=True)
-def test_bad_block_id_is_reported_not_faulted(decode_path):
-    w = W.custom(7, [40, 40], 8, 2, 64, 16)
+@pytest.mark.parametrize("kv_heads", [2, 8])
+def test_bad_block_id_is_reported_not_faulted(decode_path, kv_heads):
+    w = W.custom(7, [40, 40], 4 * kv_heads, kv_heads, 64, 16)
     t = W.make_tensors(w, DEV)
     pk.pk_get_device_error()
     bt = t["block_tables"].clone()
