@@ -16,22 +16,34 @@
 // are combined by the merge kernel.
 //
 // Per 128-token tile, inside a CTA (192 threads):
-//   warp 0  producer: reads the tile's block-table entries (one lane per
-//           page), checks them, and TMA-loads each page's K and V rows of this
-//           KV head (two 128-byte-swizzled 64-column boxes each) plus the
-//           group's 16 query rows into a 3-stage shared-memory ring;
-//   warp 1  MMA issuer (one thread): S^T[128 x 16] = K[128 x D] Q^T[D x 16]
-//           into TMEM, then, once the probabilities are written,
-//           O^T[D x 16] = V^T[D x 128] P^T[128 x 16] into TMEM;
+//   warp 0  producer: reads the tile's block-table entries one tile ahead
+//           (one lane per page), checks them, and TMA-loads each page's K rows
+//           and then V rows of this KV head (two 128-byte-swizzled 64-column
+//           boxes each) into a 3-stage shared-memory ring; K (with the
+//           group's 16 query rows, loaded only when the stage does not hold
+//           them already) and V complete separate barriers, so the scores
+//           can start while V is still landing;
+//   warp 1  MMA issuer (one thread, event loop): S^T[128 x 16] =
+//           K[128 x D] Q^T[D x 16] into TMEM as soon as a tile's K is in, and
+//           O^T[D x 16] += V^T[D x 128] P^T[128 x 16] into TMEM as soon as its
+//           probabilities are written, so neither waits for the other; O of a
+//           (sequence, head) segment accumulates in TMEM across its tiles;
 //   warps 2-5 (128 threads, thread <-> TMEM lane): read S^T (one token per
-//           thread), mask invalid tokens, take the tile max per query head
-//           (shuffles + shared memory), compute p = 2^(s - m) in fp32, round
-//           to bf16 for the MMA, keep the running denominator, and fold each
-//           tile's O^T into fp32 registers with the rescale factor
-//           (thread <-> head-dim row).
+//           thread), mask invalid tokens, compute p = 2^(s - m_ref) in fp32,
+//           round to bf16 for the MMA and keep the denominator.  m_ref is a
+//           reference max per query head that moves only when a score exceeds
+//           it by more than 2^8 (then O in TMEM and the denominator are
+//           rescaled); between moves a tile costs one OR-vote barrier.  A
+//           segment's O is read out of TMEM one tile after its last P.V was
+//           issued, normalised and stored (or written to a slot if cut).
+// Launch: the decode grid is a programmatic dependent of the previous kernel
+// in the stream (its set-up overlaps that kernel's tail; it touches global
+// memory only after it completed), and the merge grid is a programmatic
+// dependent of the decode grid.
 // Query heads are padded to the MMA's N = 16; padded columns are ignored.
 #include "decode.cuh"
 #include "sm100.cuh"
+#include "block_scan.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -63,21 +75,22 @@ constexpr uint32_t kIdescQK = idesc_bf16(kTile, kNPad, 0, 0);   // A = K (K-majo
 constexpr uint32_t kIdescPV = idesc_bf16(128, kNPad, 1, 1);     // A = V^T (MN-major), B = P^T (MN-major)
 
 struct Misc {
-    uint64_t full[kStages];
+    uint64_t full[kStages];       // K rows (and Q) of a stage landed
+    uint64_t vfull[kStages];      // V rows of a stage landed
     uint64_t empty[kStages];
     uint64_t s_full[2];
     uint64_t p_full[2];
-    uint64_t o_full[2];
+    uint64_t o_full[2];       // P.V of a tile complete (per tile parity)
+    uint64_t o_free[2];       // a segment's O buffer has been read out
     uint64_t drain;
-    int64_t scan[kThreads];
-    int64_t total;
+    int64_t scan[kThreads / 32 + 1];   // warp totals of the prologue scan
     int64_t rem0;
     int32_t s0;
     uint32_t tmem_base;
     int abort;
     int never;
     uint32_t mask[kStages][4];
-    float red[2][4][kNPad];
+    float red[4][kNPad];          // per-warp maxima when the reference max moves
     float lsum[4][kNPad];
 };
 
@@ -163,12 +176,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(&misc->full[i]), 1);
+            mbar_init(smem_u32(&misc->vfull[i]), 1);
             mbar_init(smem_u32(&misc->empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&misc->s_full[i]), 1);
-            mbar_init(smem_u32(&misc->p_full[i]), 1);
+            mbar_init(smem_u32(&misc->p_full[i]), 4);
             mbar_init(smem_u32(&misc->o_full[i]), 1);
+            mbar_init(smem_u32(&misc->o_free[i]), 4);
         }
         mbar_init(smem_u32(&misc->drain), 1);
         misc->abort = 0;
@@ -179,12 +194,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (threadIdx.x == 0 && slots) slots[2 * c].flag = 0;
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_q);
     }
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: everything above overlaps its tail; no global memory is touched
+    // before it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0 && slots) slots[2 * c].flag = 0;
+    // The merge grid may start now; it waits for this grid's completion.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- this CTA's range of the flattened tile space ----------------------
     const int per = (N + kThreads - 1) / kThreads;
@@ -196,23 +217,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int L = raw < 0 ? 0 : (raw > cap ? cap : raw);
         mine += static_cast<int64_t>((L + kTile - 1) / kTile) * Hkv;
     }
-    misc->scan[threadIdx.x] = mine;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int64_t acc = 0;
-        for (int i = 0; i < kThreads; ++i) {
-            const int64_t v = misc->scan[i];
-            misc->scan[i] = acc;
-            acc += v;
-        }
-        misc->total = acc;
-    }
-    __syncthreads();
-    const int64_t T = misc->total;
+    int64_t T;
+    const int64_t my_off = block_exclusive_scan<kThreads>(mine, misc->scan, &T);
     const int64_t beg = range_begin(c, T, C), end = range_begin(c + 1, T, C);
     const int n_tiles = static_cast<int>(end - beg);
     if (n_tiles > 0) {
-        int64_t acc = misc->scan[threadIdx.x];
+        int64_t acc = my_off;
         if (acc <= beg && beg < acc + mine) {
             for (int s = s_lo; s < s_hi; ++s) {
                 const int64_t w = static_cast<int64_t>((clamp_len(p, s, cap) + kTile - 1) / kTile) * Hkv;
@@ -248,8 +258,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         Walk w = w0;
         const int MB = p.max_blocks_per_seq;
         int issued = 0;
+        // The next tile's block-table entries are read one tile ahead, so
+        // their latency hides behind the wait for a free stage.
+        auto fetch = [&](const Walk &ww) -> int {
+            const int fp = ww.t * kTile / B;
+            return (lane < kTile / B && fp + lane < MB) ? p.block_tables[static_cast<size_t>(ww.s) * MB + fp + lane]
+                                                        : -1;
+        };
+        int phys_next = n_tiles > 0 ? fetch(w) : -1;
+        int seg_i0 = 0;
         for (int i = 0; i < n_tiles; ++i) {
+            if (i == 0 || w.t == 0) seg_i0 = i;
+            // The stage still holds this segment's queries from tile i - kStages.
+            const bool q_resident = i - seg_i0 >= kStages;
             const int st = i % kStages;
+            const int phys_raw = phys_next;
             int got = 1;
             if (lane == 0)
                 got = mbar_wait(smem_u32(&misc->empty[st]), ((i / kStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
@@ -263,11 +286,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const int tok0 = w.t * kTile;
             const int vlen = min(kTile, w.L - tok0);
             const int pages = (vlen + B - 1) / B;
-            const int first_page = tok0 / B;
             int phys = -1;
             bool ok = false;
             if (lane < pages) {
-                phys = p.block_tables[static_cast<size_t>(w.s) * MB + first_page + lane];
+                phys = phys_raw;
                 ok = phys >= 0 && phys < p.num_blocks;
                 if (!ok) set_error(p.err, PK_DEVERR_BLOCK_ID);
             }
@@ -284,47 +306,51 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const uint32_t m3 = __reduce_or_sync(0xffffffffu, word == 3 ? bits : 0u);
             const uint32_t nok = __popc(__ballot_sync(0xffffffffu, ok));
             const uint32_t full = smem_u32(&misc->full[st]);
+            const uint32_t vfull = smem_u32(&misc->vfull[st]);
             const uint32_t sbase = stage_addr + st * kStageBytes;
             if (lane == 0) {
                 misc->mask[st][0] = m0;
                 misc->mask[st][1] = m1;
                 misc->mask[st][2] = m2;
                 misc->mask[st][3] = m3;
-                mbar_arrive_expect_tx(full, nok * B * 128u * NCH * 2u + kNPad * 128u * NCH);
+                mbar_arrive_expect_tx(full, nok * B * 128u * NCH + (q_resident ? 0u : kNPad * 128u * NCH));
+                mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
             }
             __syncwarp();
-            if (ok) {
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    tma_load_4d(sbase + kKOff + ch * kChunkBytes + r0 * 128, &tm_k, full, ch * 64, w.h, 0, phys);
-                    tma_load_4d(sbase + kVOff + ch * kChunkBytes + r0 * 128, &tm_v, full, ch * 64, w.h, 0, phys);
-                }
-            }
-            if (lane == 0) {
+            // K (and Q) first: the scores can start while V is still landing.
+            if (lane == 0 && !q_resident) {
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
                     tma_load_2d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, ch * 64, w.s * H + w.h * G);
             }
+            if (ok) {
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch)
+                    tma_load_4d(sbase + kKOff + ch * kChunkBytes + r0 * 128, &tm_k, full, ch * 64, w.h, 0, phys);
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch)
+                    tma_load_4d(sbase + kVOff + ch * kChunkBytes + r0 * 128, &tm_v, vfull, ch * 64, w.h, 0, phys);
+            }
             ++issued;
             w.next(p, cap);
+            if (i + 1 < n_tiles) phys_next = fetch(w);
         }
         // On abort, let this warp's copies land before the CTA can exit.
         if (misc->abort && lane == 0) {
-            for (int i = max(0, issued - kStages); i < issued; ++i)
+            for (int i = max(0, issued - kStages); i < issued; ++i) {
                 mbar_wait(smem_u32(&misc->full[i % kStages]), (i / kStages) & 1, &misc->never, kWaitLimitNs);
+                mbar_wait(smem_u32(&misc->vfull[i % kStages]), (i / kStages) & 1, &misc->never, kWaitLimitNs);
+            }
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            bool alive = true;
-            auto pv = [&](int j) {
+            // Segment bookkeeping for P.V: O of a (sequence, head) segment
+            // accumulates in TMEM buffer (segment index & 1) across its tiles.
+            Walk wp = w0;
+            int pv_seg = -1;
+            auto pv = [&](int j, bool first, int sg) {
                 const int pb = j & 1;
-                if (!mbar_wait(smem_u32(&misc->p_full[pb]), (j >> 1) & 1, &misc->abort, kWaitLimitNs)) {
-                    misc->abort = 1;
-                    set_error(p.err, PK_DEVERR_TIMEOUT);
-                    alive = false;
-                    return;
-                }
                 tc_fence_after();
                 const uint32_t vbase = stage_addr + (j % kStages) * kStageBytes + kVOff;
                 const uint32_t pbase = p_addr + pb * kPBytes;
@@ -332,20 +358,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint64_t a = smem_desc(vbase + kk * 16 * 128, kChunkBytes, 1024, kLayoutSw128);
                     const uint64_t b = smem_desc(pbase + kk * 512, 256, 128, kLayoutNone);
-                    mma_bf16(tmem + kTmemO + pb * kNPad, a, b, kIdescPV, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + kTmemO + (sg & 1) * kNPad, a, b, kIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(smem_u32(&misc->o_full[pb]));
                 mma_commit(smem_u32(&misc->empty[j % kStages]));
             };
-            int i = 0;
-            for (; i < n_tiles && alive; ++i) {
+            // Event loop: issue P.V of a tile as soon as its probabilities are
+            // written (releasing its stage), and the scores of the next tile
+            // as soon as it has arrived; neither waits for the other.
+            auto qk = [&](int i) {
                 const int st = i % kStages;
-                if (!mbar_wait(smem_u32(&misc->full[st]), (i / kStages) & 1, &misc->abort, kWaitLimitNs)) {
-                    misc->abort = 1;
-                    set_error(p.err, PK_DEVERR_TIMEOUT);
-                    alive = false;
-                    break;
-                }
                 tc_fence_after();
                 const uint32_t sbase = stage_addr + st * kStageBytes;
                 const int sb = i & 1;
@@ -358,53 +380,129 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     mma_bf16(tmem + kTmemS + sb * kNPad, a, b, kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&misc->s_full[sb]));
-                if (i > 0) pv(i - 1);
+            };
+            int nq = 0, np = 0;
+            uint64_t t_idle = 0;
+            uint32_t spins = 0;
+            while (np < n_tiles) {
+                bool prog = false;
+                if (np < nq && mbar_test_wait(smem_u32(&misc->p_full[np & 1]), (np >> 1) & 1) &&
+                    mbar_test_wait(smem_u32(&misc->vfull[np % kStages]), (np / kStages) & 1)) {
+                    const bool first = np == 0 || wp.t == 0;
+                    const int sg = pv_seg + (first ? 1 : 0);
+                    // A new segment's O buffer must have been read out (segment sg - 2).
+                    if (!first || mbar_test_wait(smem_u32(&misc->o_free[sg & 1]), ((sg >> 1) & 1) ^ 1)) {
+                        pv(np, first, sg);
+                        pv_seg = sg;
+                        wp.next(p, cap);
+                        ++np;
+                        prog = true;
+                    }
+                }
+                if (nq < n_tiles && nq <= np + 1 &&
+                    mbar_test_wait(smem_u32(&misc->full[nq % kStages]), (nq / kStages) & 1)) {
+                    qk(nq);
+                    ++nq;
+                    prog = true;
+                }
+                if (prog) {
+                    spins = 0;
+                } else if ((++spins & 255u) == 0) {
+                    const uint64_t now = globaltimer_ns();
+                    if (spins == 256) t_idle = now;
+                    else if (misc->abort || now - t_idle > kWaitLimitNs) {
+                        misc->abort = 1;
+                        set_error(p.err, PK_DEVERR_TIMEOUT);
+                        break;
+                    }
+                }
             }
-            if (alive && n_tiles > 0) pv(n_tiles - 1);
             // Let every issued MMA finish before the CTA can release TMEM.
             mma_commit(smem_u32(&misc->drain));
             mbar_wait(smem_u32(&misc->drain), 0, &misc->never, kWaitLimitNs);
         }
         __syncwarp();
     } else {
-        // ================= softmax + correction (warps 2-5) =================
+        // ================= softmax (warps 2-5): thread <-> tile row =================
+        // A reference max per query head moves only when a score exceeds it
+        // by more than 2^8 (then O in TMEM and the denominators are rescaled);
+        // between moves p = 2^(s - m_ref) <= 2^8 and a tile costs one vote.
+        // A segment's output is read out of TMEM one tile later, when its
+        // last P.V is certainly done.
+        constexpr float kRescaleLog2 = 8.0f;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        float m_run[G], l_run[G], alpha_prev[G], o_acc[G];
+        float m_ref[G], l_run[G], m_prev[G], l_prev[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            m_run[g] = -INFINITY;
-            l_run[g] = 0.f;
-            alpha_prev[g] = 0.f;
-            o_acc[g] = 0.f;
-        }
-        bool first_corr = true;
-        int seg_t0 = 0, seg_i0 = 0;
+        for (int g = 0; g < G; ++g) m_ref[g] = l_run[g] = m_prev[g] = l_prev[g] = 0.f;
+        int seg = -1, seg_t0 = 0, seg_i0 = 0;
+        bool pending = false;            // a finished segment awaits its read-out
+        int pend_seg = 0, pend_s = 0, pend_h = 0, pend_i = 0, pend_t0 = 0, pend_i0 = 0;
+        bool pend_complete = false, pend_cut_end = false;
         Walk w = w0;
-        auto correct = [&](int j, const float (&a)[G]) -> bool {
-            const int ob = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[ob]), (j >> 1) & 1, &misc->never,
-                                                   kWaitLimitNs)))
+        auto finalize = [&]() -> bool {
+            // P.V of the segment's last tile (pend_i) complete.
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[pend_i & 1]), (pend_i >> 1) & 1,
+                                                   &misc->never, kWaitLimitNs)))
                 return false;
             tc_fence_after();
             float ov[16];
-            tmem_ld16(lane_addr + kTmemO + ob * kNPad, ov);
+            tmem_ld16(lane_addr + kTmemO + (pend_seg & 1) * kNPad, ov);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&misc->o_free[pend_seg & 1]));
 #pragma unroll
-            for (int g = 0; g < G; ++g) o_acc[g] = first_corr ? ov[g] : fmaf(o_acc[g], a[g], ov[g]);
-            first_corr = false;
+            for (int g = 0; g < G; ++g) {
+                const float v = warp_sum(l_prev[g]);
+                if (lane == 0) misc->lsum[quad][g] = v;
+            }
+            named_bar_sync(1, 128);
+            float l[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                l[g] = misc->lsum[0][g] + misc->lsum[1][g] + misc->lsum[2][g] + misc->lsum[3][g];
+            if (pend_complete) {
+                if (row < D) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        store_out(p, (static_cast<size_t>(pend_s) * H + pend_h * G + g) * D + row,
+                                  l[g] > 0.f ? ov[g] / l[g] : 0.f);
+                }
+            } else {
+                const int slot_idx = pend_i0 == 0 ? 0 : 1;
+                Slot *sl = slots + 2 * c + slot_idx;
+                if (row < D) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) sl->o[g * D + row] = ov[g];
+                }
+                if (row == 0) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        sl->m[g] = m_prev[g];
+                        sl->l[g] = l[g];
+                    }
+                    sl->s = pend_s;
+                    sl->h = pend_h;
+                    sl->start_tile = beg + pend_i0 - pend_t0;
+                    sl->total_tiles = T;
+                    // Cut at its start and finished here: this CTA merges it.
+                    if (slot_idx == 0) sl->flag = (pend_t0 > 0 && pend_cut_end) ? 1 : 0;
+                }
+            }
+            pending = false;
             return true;
         };
         for (int i = 0; i < n_tiles; ++i) {
             const bool seg_first = (i == 0) || (w.t == 0);
             const bool seg_last = (i == n_tiles - 1) || (w.t == w.nt - 1);
             if (seg_first) {
+                ++seg;
                 seg_t0 = w.t;
                 seg_i0 = i;
-                first_corr = true;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    m_run[g] = -INFINITY;
+                    m_ref[g] = -INFINITY;
                     l_run[g] = 0.f;
                 }
             }
@@ -421,34 +519,80 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             tmem_ld16(lane_addr + kTmemS + sb * kNPad, sv);
             const bool valid = (misc->mask[st][row >> 5] >> (row & 31)) & 1u;
             float s2[G];
+            bool need = false;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 s2[g] = valid ? sv[g] * p.scale_log2 : -INFINITY;
-                const float mx = warp_max(s2[g]);
-                if (lane == 0) misc->red[sb][quad][g] = mx;
+                need |= s2[g] > m_ref[g] + kRescaleLog2;
             }
-            named_bar_sync(1, 128);
-            float alpha[G];
+            if (named_bar_or(1, 128, need)) {
+                // Rare: move the reference to the running max.
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float t = fmaxf(fmaxf(misc->red[sb][0][g], misc->red[sb][1][g]),
-                                      fmaxf(misc->red[sb][2][g], misc->red[sb][3][g]));
-                const float mn = fmaxf(m_run[g], t);
-                alpha[g] = m_run[g] == -INFINITY ? 0.f : fast_exp2(m_run[g] - mn);
-                m_run[g] = mn;
+                for (int g = 0; g < G; ++g) {
+                    const float mx = warp_max(s2[g]);
+                    if (lane == 0) misc->red[quad][g] = mx;
+                }
+                named_bar_sync(1, 128);
+                float a[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float t = fmaxf(fmaxf(misc->red[0][g], misc->red[1][g]),
+                                          fmaxf(misc->red[2][g], misc->red[3][g]));
+                    const float mn = fmaxf(m_ref[g], t);
+                    a[g] = m_ref[g] == -INFINITY ? 0.f : fast_exp2(m_ref[g] - mn);
+                    l_run[g] *= a[g];
+                    m_ref[g] = mn;
+                }
+                if (!seg_first) {
+                    // O through tile i-1, in TMEM (thread <-> head-dim row).
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[(i - 1) & 1]), ((i - 1) >> 1) & 1,
+                                                           &misc->never, kWaitLimitNs))) {
+                        misc->abort = 1;
+                        set_error(p.err, PK_DEVERR_TIMEOUT);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t oaddr = lane_addr + kTmemO + (seg & 1) * kNPad;
+                    float ov[16];
+                    tmem_ld16(oaddr, ov);
+                    float lo[8], hi[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        lo[g] = g < G ? ov[g] * a[g < G ? g : 0] : ov[g];
+                        hi[g] = 8 + g < G ? ov[8 + g] * a[8 + g < G ? 8 + g : 0] : ov[8 + g];
+                    }
+                    tmem_st8(oaddr, lo);
+                    if (G > 8) tmem_st8(oaddr + 8, hi);
+                }
+                // red[] is rewritten only in a later rare path, after the next vote.
             }
             float pr[kNPad];
 #pragma unroll
             for (int g = 0; g < kNPad; ++g) pr[g] = 0.f;
 #pragma unroll
-            for (int g = 0; g < G; ++g) pr[g] = valid ? fast_exp2(s2[g] - m_run[g]) : 0.f;
+            for (int g = 0; g < G; ++g) pr[g] = valid ? fast_exp2(s2[g] - m_ref[g]) : 0.f;
             uint32_t packed[kNPad / 2];
 #pragma unroll
             for (int gp = 0; gp < kNPad / 2; ++gp) packed[gp] = pack_bf16x2(pr[2 * gp], pr[2 * gp + 1]);
             // The denominator sums the bf16 weights the MMA actually applies.
 #pragma unroll
             for (int g = 0; g < G; ++g)
-                l_run[g] = fmaf(l_run[g], alpha[g], (g & 1) ? bf16_hi(packed[g >> 1]) : bf16_lo(packed[g >> 1]));
+                l_run[g] += (g & 1) ? bf16_hi(packed[g >> 1]) : bf16_lo(packed[g >> 1]);
+            // P buffer sb is free once P.V of tile i-2 is done.
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[sb]), ((i >> 1) & 1) ^ 1, &misc->never,
+                                                   kWaitLimitNs))) {
+                misc->abort = 1;
+                set_error(p.err, PK_DEVERR_TIMEOUT);
+                break;
+            }
+            // Rows of masked tokens are zeroed once this tile's V has landed.
+            if (__any_sync(0xffffffffu, !valid) &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->vfull[st]), (i / kStages) & 1, &misc->never,
+                                                   kWaitLimitNs))) {
+                misc->abort = 1;
+                set_error(p.err, PK_DEVERR_TIMEOUT);
+                break;
+            }
             if (!valid) {
                 // The MMA multiplies every V row by its probability; rows of
                 // masked tokens may hold stale or non-finite bits, so zero them.
@@ -464,60 +608,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             *reinterpret_cast<uint4 *>(prow + 128) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar_sync(1, 128);
-            if (threadIdx.x == 64) mbar_arrive(smem_u32(&misc->p_full[sb]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&misc->p_full[sb]));
 
-            bool ok = true;
-            if (!seg_first) ok = correct(i - 1, alpha_prev);
-            if (ok && seg_last) ok = correct(i, alpha);
-            if (!ok) {
+            // The previous segment's read-out, one tile late.
+            if (pending && !finalize()) {
                 misc->abort = 1;
                 set_error(p.err, PK_DEVERR_TIMEOUT);
                 break;
             }
-#pragma unroll
-            for (int g = 0; g < G; ++g) alpha_prev[g] = alpha[g];
-
             if (seg_last) {
-                // Denominator over the 128 threads.
+                pending = true;
+                pend_seg = seg;
+                pend_s = w.s;
+                pend_h = w.h;
+                pend_i = i;
+                pend_t0 = seg_t0;
+                pend_i0 = seg_i0;
+                pend_complete = seg_t0 == 0 && w.t == w.nt - 1;
+                pend_cut_end = w.t == w.nt - 1;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float v = warp_sum(l_run[g]);
-                    if (lane == 0) misc->lsum[quad][g] = v;
+                    m_prev[g] = m_ref[g];
+                    l_prev[g] = l_run[g];
                 }
-                named_bar_sync(1, 128);
-                float l[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    l[g] = misc->lsum[0][g] + misc->lsum[1][g] + misc->lsum[2][g] + misc->lsum[3][g];
-                const bool complete = seg_t0 == 0 && w.t == w.nt - 1;
-                if (complete) {
-                    if (row < D) {
-#pragma unroll
-                        for (int g = 0; g < G; ++g)
-                            store_out(p, (static_cast<size_t>(w.s) * H + w.h * G + g) * D + row,
-                                      l[g] > 0.f ? o_acc[g] / l[g] : 0.f);
-                    }
-                } else {
-                    const int slot_idx = seg_i0 == 0 ? 0 : 1;
-                    Slot *sl = slots + 2 * c + slot_idx;
-                    if (row < D) {
-#pragma unroll
-                        for (int g = 0; g < G; ++g) sl->o[g * D + row] = o_acc[g];
-                    }
-                    if (row == 0) {
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            sl->m[g] = m_run[g];
-                            sl->l[g] = l[g];
-                        }
-                        sl->s = w.s;
-                        sl->h = w.h;
-                        sl->start_tile = beg + seg_i0 - seg_t0;
-                        sl->total_tiles = T;
-                        // Cut at its start and finished here: this CTA merges it.
-                        if (slot_idx == 0) sl->flag = (seg_t0 > 0 && w.t == w.nt - 1) ? 1 : 0;
-                    }
+                if (i == n_tiles - 1 && !finalize()) {
+                    misc->abort = 1;
+                    set_error(p.err, PK_DEVERR_TIMEOUT);
+                    break;
                 }
             }
             w.next(p, cap);
@@ -537,38 +655,74 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 template <int D, int G>
 __global__ void __launch_bounds__(128)
 decode_tc_merge_kernel(const DecodeParams p, int C) {
+    // Launched as a programmatic dependent of the decode grid: wait for it
+    // to finish and its writes to be visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const Slot *slots = static_cast<const Slot *>(p.tc_slots);
     const int c = blockIdx.x;
+    const int d = threadIdx.x < D ? threadIdx.x : D - 1;
     const Slot *mine = slots + 2 * c;
-    if (mine->flag != 1) return;
+    // Everything the common case needs (this CTA's slot 0 and both slots of
+    // CTA c - 1) is loaded at once, before the flag is known.
+    const Slot *q0 = slots + 2 * (c > 0 ? c - 1 : c);
+    const Slot *q1 = q0 + 1;
+    const int flag = mine->flag;
     const int s = mine->s, h = mine->h;
     const int64_t start = mine->start_tile, T = mine->total_tiles;
+    float mm[G], ml[G], mo[G], am[G], al[G], ao[G], bm[G], bl[G], bo[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        mm[g] = mine->m[g];
+        ml[g] = mine->l[g];
+        mo[g] = mine->o[g * D + d];
+        am[g] = q0->m[g];
+        al[g] = q0->l[g];
+        ao[g] = q0->o[g * D + d];
+        bm[g] = q1->m[g];
+        bl[g] = q1->l[g];
+        bo[g] = q1->o[g * D + d];
+    }
+    if (flag != 1 || threadIdx.x >= D) return;
     int ca = static_cast<int>(start * C / T);
     while (ca + 1 < C && range_begin(ca + 1, T, C) <= start) ++ca;
-    // Contributors are the CTAs from ca to c with a non-empty range (when the
-    // grid has more CTAs than tiles, some ranges are empty and hold no slot).
-    float M[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) M[g] = -INFINITY;
-    for (int cc = ca; cc <= c; ++cc) {
-        if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
-        const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
-#pragma unroll
-        for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], sl->m[g]);
-    }
-    const int d = threadIdx.x;
-    if (d >= D) return;
     float num[G], den[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) num[g] = den[g] = 0.f;
-    for (int cc = ca; cc <= c; ++cc) {
-        if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
-        const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
+    if (ca == c - 1) {
+        // Two parts: CTA c - 1 (slot 0 if the segment is its first, else 1) and this CTA.
+        const bool first_of_prev = range_begin(c - 1, T, C) >= start;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const float a = rescale(sl->m[g], M[g]);
-            den[g] = fmaf(a, sl->l[g], den[g]);
-            num[g] = fmaf(a, sl->o[g * D + d], num[g]);
+            const float pm = first_of_prev ? am[g] : bm[g];
+            const float pl = first_of_prev ? al[g] : bl[g];
+            const float po = first_of_prev ? ao[g] : bo[g];
+            const float M = fmaxf(pm, mm[g]);
+            const float a0 = rescale(pm, M), a1 = rescale(mm[g], M);
+            den[g] = a0 * pl + a1 * ml[g];
+            num[g] = a0 * po + a1 * mo[g];
+        }
+    } else {
+        // Contributors are the CTAs from ca to c with a non-empty range (when
+        // the grid has more CTAs than tiles, some ranges are empty and hold
+        // no slot).
+        float M[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) M[g] = -INFINITY;
+        for (int cc = ca; cc <= c; ++cc) {
+            if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
+            const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
+#pragma unroll
+            for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], sl->m[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) num[g] = den[g] = 0.f;
+        for (int cc = ca; cc <= c; ++cc) {
+            if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
+            const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float a = rescale(sl->m[g], M[g]);
+                den[g] = fmaf(a, sl->l[g], den[g]);
+                num[g] = fmaf(a, sl->o[g * D + d], num[g]);
+            }
         }
     }
 #pragma unroll
@@ -631,12 +785,22 @@ cudaError_t launch_dg(const CUtensorMap &mk, const CUtensorMap &mv, const CUtens
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    decode_tc_kernel<D, G><<<C, kThreads, kSmemBytes, stream>>>(mk, mv, mq, p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, G>, mk, mv, mq, p);
     if (e != cudaSuccess) return e;
     if (!p.tc_slots) return cudaSuccess;   // no sequence longer than one tile: nothing is cut
-    decode_tc_merge_kernel<D, G><<<C, 128, 0, stream>>>(p, C);
-    return cudaGetLastError();
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, decode_tc_merge_kernel<D, G>, p, C);
 }
 
 template <int D>

@@ -43,6 +43,18 @@ SM100_DEV uint64_t globaltimer_ns() {
     return t;
 }
 
+// Non-blocking probe of an mbarrier phase (true once the phase with the
+// given parity has completed).
+SM100_DEV bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete, giving up
 // after `limit_ns` of wall time or when *abort becomes non-zero.  Returns
 // false on give-up.
