@@ -19,6 +19,9 @@ reshape_and_cache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ 
                          uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                          const int64_t *__restrict__ slot_mapping, int num_tokens,
                          int row_vecs, int64_t num_slots, unsigned int *err) {
+    // A decode grid launched as this grid's programmatic dependent may start
+    // its set-up now; it reads the cache only after this grid has completed.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t t = i / row_vecs;
     const int e = static_cast<int>(i - t * row_vecs);
@@ -43,6 +46,7 @@ __global__ void __launch_bounds__(kThreads)
 copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                    const int64_t *__restrict__ pairs, int64_t block_vecs, int num_blocks,
                    unsigned int *err) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // as in reshape_and_cache_kernel
     const int pair = blockIdx.x;
     const int64_t src = pairs[2 * pair];
     const int64_t dst = pairs[2 * pair + 1];
