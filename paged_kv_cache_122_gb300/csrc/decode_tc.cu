@@ -22,7 +22,9 @@
 //           boxes each) into a 3-stage shared-memory ring; K (with the
 //           group's 16 query rows, loaded only when the stage does not hold
 //           them already) and V complete separate barriers, so the scores
-//           can start while V is still landing;
+//           can start while V is still landing; the tile's position
+//           (sequence, head, tile, tiles in segment) goes with the stage, so
+//           the other roles never walk the sequence lengths themselves;
 //   warp 1  MMA issuer (one thread, event loop): S^T[128 x 16] =
 //           K[128 x D] Q^T[D x 16] into TMEM as soon as a tile's K is in, and
 //           O^T[D x 16] += V^T[D x 128] P^T[128 x 16] into TMEM as soon as its
@@ -90,6 +92,7 @@ struct Misc {
     int abort;
     int never;
     uint32_t mask[kStages][4];
+    int4 meta[kStages];            // (sequence, KV head, tile, tiles in segment) of a stage's tile
     float red[4][kNPad];          // per-warp maxima when the reference max moves
     float lsum[4][kNPad];
 };
@@ -313,6 +316,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 misc->mask[st][1] = m1;
                 misc->mask[st][2] = m2;
                 misc->mask[st][3] = m3;
+                misc->meta[st] = make_int4(w.s, w.h, w.t, w.nt);
                 mbar_arrive_expect_tx(full, nok * B * 128u * NCH + (q_resident ? 0u : kNPad * 128u * NCH));
                 mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
             }
@@ -347,7 +351,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         if (lane == 0) {
             // Segment bookkeeping for P.V: O of a (sequence, head) segment
             // accumulates in TMEM buffer (segment index & 1) across its tiles.
-            Walk wp = w0;
             int pv_seg = -1;
             auto pv = [&](int j, bool first, int sg) {
                 const int pb = j & 1;
@@ -388,13 +391,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 bool prog = false;
                 if (np < nq && mbar_test_wait(smem_u32(&misc->p_full[np & 1]), (np >> 1) & 1) &&
                     mbar_test_wait(smem_u32(&misc->vfull[np % kStages]), (np / kStages) & 1)) {
-                    const bool first = np == 0 || wp.t == 0;
+                    const bool first = np == 0 || misc->meta[np % kStages].z == 0;
                     const int sg = pv_seg + (first ? 1 : 0);
                     // A new segment's O buffer must have been read out (segment sg - 2).
                     if (!first || mbar_test_wait(smem_u32(&misc->o_free[sg & 1]), ((sg >> 1) & 1) ^ 1)) {
                         pv(np, first, sg);
                         pv_seg = sg;
-                        wp.next(p, cap);
                         ++np;
                         prog = true;
                     }
@@ -440,7 +442,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         bool pending = false;            // a finished segment awaits its read-out
         int pend_seg = 0, pend_s = 0, pend_h = 0, pend_i = 0, pend_t0 = 0, pend_i0 = 0;
         bool pend_complete = false, pend_cut_end = false;
-        Walk w = w0;
         auto finalize = [&]() -> bool {
             // P.V of the segment's last tile (pend_i) complete.
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[pend_i & 1]), (pend_i >> 1) & 1,
@@ -494,18 +495,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             return true;
         };
         for (int i = 0; i < n_tiles; ++i) {
-            const bool seg_first = (i == 0) || (w.t == 0);
-            const bool seg_last = (i == n_tiles - 1) || (w.t == w.nt - 1);
-            if (seg_first) {
-                ++seg;
-                seg_t0 = w.t;
-                seg_i0 = i;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    m_ref[g] = -INFINITY;
-                    l_run[g] = 0.f;
-                }
-            }
             const int st = i % kStages;
             const int sb = i & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->s_full[sb]), (i >> 1) & 1, &misc->never,
@@ -513,6 +502,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 misc->abort = 1;
                 set_error(p.err, PK_DEVERR_TIMEOUT);
                 break;
+            }
+            const int4 mt = misc->meta[st];   // (s, h, t, nt), written with the stage
+            const bool seg_first = (i == 0) || (mt.z == 0);
+            const bool seg_last = (i == n_tiles - 1) || (mt.z == mt.w - 1);
+            if (seg_first) {
+                ++seg;
+                seg_t0 = mt.z;
+                seg_i0 = i;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    m_ref[g] = -INFINITY;
+                    l_run[g] = 0.f;
+                }
             }
             tc_fence_after();
             float sv[16];
@@ -620,13 +622,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (seg_last) {
                 pending = true;
                 pend_seg = seg;
-                pend_s = w.s;
-                pend_h = w.h;
+                pend_s = mt.x;
+                pend_h = mt.y;
                 pend_i = i;
                 pend_t0 = seg_t0;
                 pend_i0 = seg_i0;
-                pend_complete = seg_t0 == 0 && w.t == w.nt - 1;
-                pend_cut_end = w.t == w.nt - 1;
+                pend_complete = seg_t0 == 0 && mt.z == mt.w - 1;
+                pend_cut_end = mt.z == mt.w - 1;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     m_prev[g] = m_ref[g];
@@ -638,7 +640,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     break;
                 }
             }
-            w.next(p, cap);
         }
         tc_fence_before();
     }
