@@ -164,6 +164,69 @@ print(json.dumps({{"times": times, "bytes": nbytes, "seqs": len(sel), "tokens": 
 """
 
 
+BM_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+try:
+    os.sched_setaffinity(0, {{sorted(os.sched_getaffinity(0))[0]}})
+except Exception:
+    pass
+from paged_kv_cache_122_gb300 import BlockManager, workloads as W
+w = W.get({workload!r}, {seed})
+N, B, K = w.num_seqs, w.block_size, {steps}
+lens = [int(x) for x in w.seq_lens]
+MB = -(-(max(lens) + K) // B)
+ids = np.arange(N, dtype=np.int64)
+def native():
+    bm = BlockManager(w.num_blocks + N * (K // B + 2), B)
+    for s in range(N):
+        bm.add_sequence(s)
+        bm.append_slots(np.full(lens[s], s, dtype=np.int64))
+    tables = np.empty((N, MB), dtype=np.int32); sl = np.empty(N, dtype=np.int32)
+    ts = []
+    for _ in range(K):
+        t0 = time.perf_counter()
+        bm.append_slots(ids); bm.take_copies(); bm.export(ids, MB, tables, sl)
+        ts.append(time.perf_counter() - t0)
+    return ts
+def reference():
+    import oracle
+    bm = oracle.CowBlockManager(w.num_blocks + N * (K // B + 2), B)
+    for s in range(N):
+        bm.new_sequence(str(s))
+        for _ in range(lens[s]):
+            bm.append_slot(str(s))
+    ts = []
+    for _ in range(K):
+        t0 = time.perf_counter()
+        slots = [bm.append_slot(str(s)) for s in range(N)]
+        pairs = bm.take_copies()
+        tables = np.full((N, MB), -1, dtype=np.int32)
+        for s in range(N):
+            tb = bm.tables[str(s)]
+            tables[s, :len(tb)] = tb
+        sl = np.array([bm.lengths[str(s)] for s in range(N)], dtype=np.int32)
+        ts.append(time.perf_counter() - t0)
+    return ts
+out = {{"native": native()}}
+if {with_oracle}:
+    out["oracle"] = reference()
+print(json.dumps(out))
+"""
+
+
+def run_block_manager(workload: str, seed: int, steps: int, with_oracle: bool):
+    """Host block-manager time of one decode step (append every sequence, take
+    the copy pairs, export tables and lengths), on one pinned host core."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    code = BM_SNIPPET.format(root=ROOT, workload=workload, seed=seed, steps=steps, with_oracle=with_oracle)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if res.returncode != 0:
+        raise RuntimeError(f"block-manager timing failed:\n{res.stderr[-2000:]}")
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
 def run_cpu_oracle(workload: str, seed: int, nseq: int, budget_s: float, max_reps: int = 1000):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -440,6 +503,17 @@ def run_ours(args):
     }
     if others:
         res["other_workloads"] = others
+    if rank == 0:
+        r = run_block_manager(args.workload, args.seed, 50, not args.no_cpu_baseline)
+        nat = statistics.median(r["native"]) * 1e6
+        bmr = {"what": f"host block manager, one decode step of {w.num_seqs} sequences: append a slot to "
+                       "each, take the copy pairs, export tables and lengths (one pinned core, median of 50)",
+               "native_us_per_step": round(nat, 2),
+               "appends_per_s": round(w.num_seqs / (nat * 1e-6), 1)}
+        if "oracle" in r:
+            ref_us = statistics.median(r["oracle"]) * 1e6
+            bmr["cpu_baseline"] = {"kind": "oracle", "us_per_step": round(ref_us, 2), "cores": 1}
+        res["block_manager"] = bmr
     if not args.no_cpu_baseline:
         r = run_cpu_oracle(args.workload, args.seed, args.cpu_seqs, args.cpu_budget)
         tot = sum(r["times"])

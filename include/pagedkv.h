@@ -63,7 +63,12 @@ enum pk_status {
     PK_ERR_WORKSPACE = -4,     /* workspace missing or smaller than required */
     PK_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
     PK_ERR_ALIGNMENT = -6,     /* a pointer is not 16-byte aligned */
-    PK_ERR_NO_DEVICE = -7      /* no usable CUDA device */
+    PK_ERR_NO_DEVICE = -7,     /* no usable CUDA device */
+    /* Host block manager (pagedkv_block_manager.h) only: */
+    PK_ERR_NO_BLOCKS = -8,     /* the pool has no free block left: the scheduler must preempt */
+    PK_ERR_UNKNOWN_SEQUENCE = -9,  /* no sequence with that id */
+    PK_ERR_SEQUENCE_EXISTS = -10,  /* a sequence with that id already exists */
+    PK_ERR_HOST_MEMORY = -11   /* a host allocation failed */
 };
 
 enum pk_dtype { PK_BF16 = 0, PK_FP32 = 1 };

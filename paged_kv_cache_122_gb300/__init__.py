@@ -7,7 +7,9 @@ The calls follow the pages' statement of the problem:
 * ``copy_blocks(k_cache, v_cache, src_dst_pairs)``
 
 All work runs in the library's sm_103a kernels (``csrc/``); PyTorch supplies
-device memory and streams.  Importing the package does not load the library;
+device memory and streams.  ``BlockManager`` is the library's host-side C++
+block manager (free list, block tables, copy-on-write) that produces the
+slot mapping, copy pairs and tables of a decode step.  Importing the package does not load the library;
 the first call does, and fails loudly if it has not been built.
 """
 from .api import (  # noqa: F401
@@ -23,3 +25,4 @@ from .api import (  # noqa: F401
     reshape_and_cache,
 )
 from ._native import PagedKVError, load as load_library  # noqa: F401
+from .block_manager import BlockManager  # noqa: F401

@@ -39,6 +39,20 @@ SIGNATURES = {
         c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "pk_get_device_error": (c_int, [ctypes.POINTER(c_uint), c_void_p]),
     "pk_set_decode_path": (c_int, [c_int]),
+    # include/pagedkv_block_manager.h
+    "pk_bm_create": (c_void_p, [c_int, c_int]),
+    "pk_bm_destroy": (None, [c_void_p]),
+    "pk_bm_add_sequence": (c_int, [c_void_p, ctypes.c_int64]),
+    "pk_bm_append_slots": (c_int, [c_void_p, c_void_p, c_int, c_void_p]),
+    "pk_bm_fork": (c_int, [c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
+    "pk_bm_free_sequence": (c_int, [c_void_p, ctypes.c_int64]),
+    "pk_bm_num_pending_copies": (c_int, [c_void_p]),
+    "pk_bm_take_copies": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(c_int)]),
+    "pk_bm_export": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p]),
+    "pk_bm_sequence_info": (c_int, [c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
+                                    ctypes.POINTER(c_int)]),
+    "pk_bm_num_free_blocks": (c_int, [c_void_p]),
+    "pk_bm_blocks_in_use": (c_int, [c_void_p]),
 }
 
 PK_OK = 0
@@ -46,7 +60,10 @@ PK_BF16, PK_FP32 = 0, 1
 STATUS_NAMES = {
     0: "PK_OK", -1: "PK_ERR_NULL", -2: "PK_ERR_SHAPE", -3: "PK_ERR_UNSUPPORTED",
     -4: "PK_ERR_WORKSPACE", -5: "PK_ERR_CUDA", -6: "PK_ERR_ALIGNMENT", -7: "PK_ERR_NO_DEVICE",
+    -8: "PK_ERR_NO_BLOCKS", -9: "PK_ERR_UNKNOWN_SEQUENCE", -10: "PK_ERR_SEQUENCE_EXISTS",
+    -11: "PK_ERR_HOST_MEMORY",
 }
+PK_ERR_NO_BLOCKS, PK_ERR_UNKNOWN_SEQUENCE, PK_ERR_SEQUENCE_EXISTS = -8, -9, -10
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_TENSOR_CORE_HEAD_BATCHED = 0, 1, 2, 3
 

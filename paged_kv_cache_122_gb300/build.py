@@ -1,7 +1,8 @@
 """Compile the CUDA sources into ``lib/libpagedkv.so`` (sm_103a only).
 
-Every ``csrc/*.cu`` file is compiled in parallel with nvcc, then linked into one
-shared library with a C ABI (``include/pagedkv.h``).  The CUDA runtime is linked
+Every ``csrc/*.cu`` file (and the host-only ``csrc/*.cpp`` files) is compiled
+in parallel with nvcc, then linked into one shared library with a C ABI
+(``include/pagedkv.h``, ``include/pagedkv_block_manager.h``).  The CUDA runtime is linked
 statically, so the library needs only the driver at run time.
 """
 from __future__ import annotations
@@ -35,7 +36,7 @@ def nvcc() -> str:
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _newest_input() -> float:
@@ -58,7 +59,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None, jobs: in
     extra = list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OBJDIR, os.path.basename(src).replace(".", "_") + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:

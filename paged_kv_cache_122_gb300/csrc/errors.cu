@@ -66,6 +66,10 @@ extern "C" const char *pk_status_string(int status) {
         case PK_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
         case PK_ERR_ALIGNMENT: return "a device pointer is not 16-byte aligned";
         case PK_ERR_NO_DEVICE: return "no usable CUDA device";
+        case PK_ERR_NO_BLOCKS: return "no free block left in the pool";
+        case PK_ERR_UNKNOWN_SEQUENCE: return "no sequence with that id";
+        case PK_ERR_SEQUENCE_EXISTS: return "a sequence with that id already exists";
+        case PK_ERR_HOST_MEMORY: return "a host allocation failed";
         default: return "unknown status";
     }
 }

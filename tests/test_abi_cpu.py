@@ -13,6 +13,8 @@ from conftest import ROOT
 from paged_kv_cache_122_gb300 import _native, build
 
 HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 NULL = None
 
 
@@ -23,14 +25,17 @@ def lib():
     return _native.load()
 
 
-def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pk_[a-z_0-9]+)\s*\(", text)))
+def _declared_functions(headers=None):
+    names = set()
+    for h in headers or HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(pk_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_three_step_calls():
-    names = _declared_functions()
+    names = _declared_functions([HEADER])
     for n in ("pk_paged_attention_decode", "pk_reshape_and_cache", "pk_copy_blocks",
               "pk_decode_workspace_bytes", "pk_gather_kv", "pk_get_device_error", "pk_status_string"):
         assert n in names
