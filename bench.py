@@ -327,6 +327,72 @@ def workload_report(name, seed, dev, steps, flush, peak):
     return rep
 
 
+def multi_layer_report(w, t, dev, layers, steps, workspace, out, peak):
+    """One attention step of a `layers`-layer model (the Llama-3-70B batch has
+    80): the copy-on-write copies and the append of every layer in one launch
+    each, then one decode per layer over that layer's own caches.  Layer 0 is
+    the workload's cache; the others are filled on the GPU (values do not
+    matter for timing; parity is in the tests).  The caches (GBs per layer)
+    far exceed L2, so no flush is needed."""
+    import torch
+    import paged_kv_cache_122_gb300 as pk
+    from paged_kv_cache_122_gb300 import metrics as M
+    gen = torch.Generator(device=dev).manual_seed(4321)
+    kcs, vcs = [t["k_cache"]], [t["v_cache"]]
+    for _ in range(layers - 1):
+        kcs.append(torch.randn(t["k_cache"].shape, generator=gen, device=dev, dtype=torch.bfloat16))
+        vcs.append(torch.randn(t["v_cache"].shape, generator=gen, device=dev, dtype=torch.bfloat16))
+    lk, lv = pk.LayerPointers(kcs), pk.LayerPointers(vcs)
+    lkn, lvn = pk.LayerPointers([t["k_new"]] * layers), pk.LayerPointers([t["v_new"]] * layers)
+    stream = torch.cuda.current_stream(dev)
+
+    def prelude():
+        if w.copy_pairs.shape[0]:
+            pk.pk_copy_blocks_layers(lk, lv, t["copy_pairs"])
+        if w.num_new_tokens:
+            pk.pk_reshape_and_cache_layers(lkn, lvn, lk, lv, t["slot_mapping"])
+
+    def prelude_per_layer():
+        for l in range(layers):
+            if w.copy_pairs.shape[0]:
+                pk.copy_blocks(kcs[l], vcs[l], t["copy_pairs"])
+            if w.num_new_tokens:
+                pk.reshape_and_cache(t["k_new"], t["v_new"], kcs[l], vcs[l], t["slot_mapping"])
+
+    def decode_all():
+        for l in range(layers):
+            pk.pk_paged_attention_decode(out, t["q"], kcs[l], vcs[l], t["block_tables"], t["seq_lens"], w.scale,
+                                         w.block_size, w.max_seq_len, workspace)
+
+    prelude(); decode_all(); prelude_per_layer()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream); prelude(); e[1].record(stream); decode_all(); e[2].record(stream)
+    pl = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in pl:
+        e[0].record(stream); prelude_per_layer(); e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    assert pk.pk_get_device_error(dev) == 0
+    step = statistics.median(e[0].elapsed_time(e[2]) for e in ev)
+    app = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    dec = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    app_pl = statistics.median(e[0].elapsed_time(e[1]) for e in pl)
+    ub = M.useful_bytes(w)
+    gbs = ub["attention"] * layers / (dec * 1e-3) / 1e9
+    rep = {"layers": layers, "step_ms": round(step, 3),
+           "what": "copy + append of all layers in one launch each, then one decode per layer (median of "
+                   f"{steps} steps; {layers} separate K/V caches of {w.num_blocks} blocks)",
+           "decode_ms_per_layer": round(dec / layers, 4), "decode_gbs": round(gbs, 1),
+           "decode_frac": round(gbs / peak, 4),
+           "append_all_layers_one_launch_us": round(app * 1e3, 2),
+           "append_per_layer_launches_us": round(app_pl * 1e3, 2),
+           "tokens_per_s_all_layers": round(w.num_seqs / (step * 1e-3), 1)}
+    del kcs, vcs, lk, lv
+    torch.cuda.empty_cache()
+    return rep
+
+
 def run_ours(args):
     import torch
     import paged_kv_cache_122_gb300 as pk
@@ -430,6 +496,11 @@ def run_ours(args):
             if name != args.workload:
                 others[name] = workload_report(name, args.seed, dev, 20, flush, peak0)
 
+    multi = None
+    if args.layers > 1 and rank == 0:
+        peak0, _ = load_peaks()
+        multi = multi_layer_report(w, t, dev, args.layers, 5, workspace, out, peak0)
+
     if ws > 1:
         total_ms, e2e_ms, all_bytes = aggregate_over_ranks(total_ms, e2e_ms, float(ub["step"]), dev)
     else:
@@ -503,6 +574,8 @@ def run_ours(args):
     }
     if others:
         res["other_workloads"] = others
+    if multi:
+        res["multi_layer"] = multi
     if rank == 0:
         r = run_block_manager(args.workload, args.seed, 50, not args.no_cpu_baseline)
         nat = statistics.median(r["native"]) * 1e6
@@ -575,6 +648,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--report-workloads", action="store_true",
                     help="also time decode alone on the other workloads (extra context in the line)")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="also time one attention step of a model with this many layers (separate caches; "
+                         "multi-layer copy/append launches), e.g. 80 for Llama-3-70B")
     ap.add_argument("--cpu-seqs", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-seqs", type=int, default=32)

@@ -81,6 +81,8 @@ enum pk_dtype { PK_BF16 = 0, PK_FP32 = 1 };
                                    max_blocks_per_seq * block_size */
 #define PK_DEVERR_TIMEOUT  0x10u /* a kernel gave up waiting on one of its own pipeline
                                     barriers (never expected; the results are invalid) */
+#define PK_DEVERR_POINTER  0x20u /* a per-layer pointer of a *_layers call is NULL or not
+                                    16-byte aligned (that layer was skipped) */
 
 /* Human-readable name of a pk_status value; never NULL. */
 const char *pk_status_string(int status);
@@ -241,6 +243,39 @@ int pk_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_ca
 int pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
                    int num_pairs, int num_kv_heads, int head_dim, int num_blocks,
                    int block_size, pk_stream_t stream);
+
+/*
+ * Multi-layer variants: the same append / block copy on every layer of a
+ * model in ONE launch.  A model keeps two cache tensors per layer
+ * ("PagedAttention from First Principles", §5 "The PagedAttention
+ * algorithm"), a logical block costs one physical block in every layer (§6
+ * "The block table, byte by byte": 80 layers of Llama-3-70B), so the slots
+ * of a step and the copy-on-write pairs are the same for all layers.
+ *
+ *   k_layers, v_layers   DEVICE array of num_layers DEVICE pointers, layer l's
+ *                        new K (V) rows [num_tokens, num_kv_heads, head_dim] bf16
+ *   k_cache_layers, v_cache_layers
+ *                        DEVICE array of num_layers DEVICE pointers, layer l's
+ *                        cache [num_blocks, block_size, num_kv_heads, head_dim]
+ *   slot_mapping, src_dst_pairs, sizes: as in the one-layer calls, shared by
+ *                        every layer.
+ *
+ * The pointer arrays are caller-owned device memory (8-byte aligned); the
+ * host cannot read them, so a NULL or unaligned per-layer pointer is found on
+ * the GPU: that layer is skipped and PK_DEVERR_POINTER is set.  Bad slots and
+ * pairs are handled per layer as in the one-layer calls.  num_layers in
+ * [1, 65535] (block copies: [1, 32767]); num_layers == 0 or no tokens / pairs
+ * is a no-op.  Bit-exact.
+ */
+int pk_reshape_and_cache_layers(const void *const *k_layers, const void *const *v_layers,
+                                void *const *k_cache_layers, void *const *v_cache_layers,
+                                const int64_t *slot_mapping, int num_tokens, int num_layers,
+                                int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                pk_stream_t stream);
+int pk_copy_blocks_layers(void *const *k_cache_layers, void *const *v_cache_layers,
+                          const int64_t *src_dst_pairs, int num_pairs, int num_layers,
+                          int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                          pk_stream_t stream);
 
 /*
  * Gather every sequence's K/V through its block table into contiguous rows:

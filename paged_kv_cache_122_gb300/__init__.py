@@ -13,14 +13,17 @@ slot mapping, copy pairs and tables of a decode step.  Importing the package doe
 the first call does, and fails loudly if it has not been built.
 """
 from .api import (  # noqa: F401
+    LayerPointers,
     copy_blocks,
     paged_attention_decode,
     pk_copy_blocks,
+    pk_copy_blocks_layers,
     pk_decode_workspace_bytes,
     pk_gather_kv,
     pk_get_device_error,
     pk_paged_attention_decode,
     pk_reshape_and_cache,
+    pk_reshape_and_cache_layers,
     pk_set_decode_path,
     reshape_and_cache,
 )

@@ -33,6 +33,11 @@ SIGNATURES = {
         c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "pk_copy_blocks": (c_int, [
         c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "pk_reshape_and_cache_layers": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+        c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "pk_copy_blocks_layers": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "pk_gather_kv": (c_int, [
         c_void_p, c_void_p, c_void_p, c_void_p,
         c_void_p, c_int, c_void_p, c_void_p, c_int,
@@ -65,6 +70,7 @@ STATUS_NAMES = {
 }
 PK_ERR_NO_BLOCKS, PK_ERR_UNKNOWN_SEQUENCE, PK_ERR_SEQUENCE_EXISTS = -8, -9, -10
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
+DEVERR_POINTER = 0x20
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_TENSOR_CORE_HEAD_BATCHED = 0, 1, 2, 3
 
 _lib = None

@@ -8,7 +8,7 @@ the pages' spelling of the same calls.
 from __future__ import annotations
 
 import ctypes
-from typing import Optional, Tuple
+from typing import Optional, Sequence, Tuple
 
 import torch
 
@@ -157,6 +157,73 @@ def pk_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: 
 
 
 copy_blocks = pk_copy_blocks
+
+
+class LayerPointers:
+    """A device array of the data pointers of per-layer tensors (what the
+    ``*_layers`` calls take).  Build it once per set of layers: it holds a
+    reference to the tensors so that their memory stays alive."""
+
+    def __init__(self, tensors: Sequence[torch.Tensor]):
+        tensors = list(tensors)
+        if not tensors:
+            raise ValueError("need at least one layer")
+        dev = tensors[0].device
+        shape = tuple(tensors[0].shape)
+        for i, t in enumerate(tensors):
+            _need(t, f"layer {i}", torch.bfloat16, len(shape), dev)
+            if tuple(t.shape) != shape:
+                raise ValueError("every layer must have the same shape")
+        self.tensors = tensors
+        self.shape = shape
+        self.device = dev
+        self.ptrs = torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=dev)
+
+    def __len__(self):
+        return len(self.tensors)
+
+
+def _layers(x) -> LayerPointers:
+    return x if isinstance(x, LayerPointers) else LayerPointers(x)
+
+
+def pk_reshape_and_cache_layers(k_layers, v_layers, k_cache_layers, v_cache_layers,
+                                slot_mapping: torch.Tensor, stream=None) -> None:
+    """The append of every layer in one launch: layer l's new rows go to layer
+    l's caches at the shared slots.  Arguments are lists of per-layer tensors
+    or prebuilt ``LayerPointers``.  See the C header."""
+    k, v, kc, vc = (_layers(x) for x in (k_layers, v_layers, k_cache_layers, v_cache_layers))
+    n = len(k)
+    if not (len(v) == len(kc) == len(vc) == n):
+        raise ValueError("every argument needs the same number of layers")
+    dev = kc.device
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    if len(k.shape) != 3 or len(kc.shape) != 4 or v.shape != k.shape or vc.shape != kc.shape:
+        raise ValueError("layers must be [T, Hkv, D] rows and [P, B, Hkv, D] caches")
+    T, Hkv, D = k.shape
+    P, B, Hc, Dc = kc.shape
+    if (Hc, Dc) != (Hkv, D) or slot_mapping.shape[0] != T:
+        raise ValueError("k / cache / slot_mapping shapes disagree")
+    with torch.cuda.device(dev):
+        st = load().pk_reshape_and_cache_layers(_ptr(k.ptrs), _ptr(v.ptrs), _ptr(kc.ptrs), _ptr(vc.ptrs),
+                                                _ptr(slot_mapping), T, n, Hkv, D, P, B, _stream(dev, stream))
+    check("pk_reshape_and_cache_layers", st)
+
+
+def pk_copy_blocks_layers(k_cache_layers, v_cache_layers, src_dst_pairs: torch.Tensor, stream=None) -> None:
+    """The copy-on-write block copies of every layer in one launch.  See the C header."""
+    kc, vc = _layers(k_cache_layers), _layers(v_cache_layers)
+    if len(kc) != len(vc) or kc.shape != vc.shape or len(kc.shape) != 4:
+        raise ValueError("k / v cache layers disagree")
+    dev = kc.device
+    _need(src_dst_pairs, "src_dst_pairs", torch.int64, 2, dev)
+    if src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [n, 2]")
+    P, B, Hkv, D = kc.shape
+    with torch.cuda.device(dev):
+        st = load().pk_copy_blocks_layers(_ptr(kc.ptrs), _ptr(vc.ptrs), _ptr(src_dst_pairs), src_dst_pairs.shape[0],
+                                          len(kc), Hkv, D, P, B, _stream(dev, stream))
+    check("pk_copy_blocks_layers", st)
 
 
 def pk_gather_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

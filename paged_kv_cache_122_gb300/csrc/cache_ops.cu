@@ -72,6 +72,79 @@ copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
     }
 }
 
+// Multi-layer variants: blockIdx.y selects the layer (copy: layer * 2 + K/V);
+// each layer's pointers come from caller-owned device arrays and are checked
+// here, where they can be read.
+__device__ __forceinline__ bool usable(const void *ptr) {
+    return ptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0;
+}
+
+__global__ void __launch_bounds__(kThreads)
+reshape_and_cache_layers_kernel(const uint4 *const *k_layers, const uint4 *const *v_layers,
+                                uint4 *const *k_cache_layers, uint4 *const *v_cache_layers,
+                                const int64_t *__restrict__ slot_mapping, int num_tokens,
+                                int row_vecs, int64_t num_slots, unsigned int *err) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // as in reshape_and_cache_kernel
+    const int layer = blockIdx.y;
+    const uint4 *k = k_layers[layer];
+    const uint4 *v = v_layers[layer];
+    uint4 *kc = k_cache_layers[layer];
+    uint4 *vc = v_cache_layers[layer];
+    if (!usable(k) || !usable(v) || !usable(kc) || !usable(vc)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) pk::set_error(err, PK_DEVERR_POINTER);
+        return;
+    }
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t t = i / row_vecs;
+    const int e = static_cast<int>(i - t * row_vecs);
+    if (t >= num_tokens) return;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (e == 0) pk::set_error(err, PK_DEVERR_SLOT);
+        return;
+    }
+    const uint4 kv = pk::ldg_stream(k + t * row_vecs + e);
+    const uint4 vv = pk::ldg_stream(v + t * row_vecs + e);
+    kc[slot * row_vecs + e] = kv;
+    vc[slot * row_vecs + e] = vv;
+}
+
+__global__ void __launch_bounds__(kThreads)
+copy_blocks_layers_kernel(uint4 *const *k_cache_layers, uint4 *const *v_cache_layers,
+                          const int64_t *__restrict__ pairs, int64_t block_vecs, int num_blocks,
+                          unsigned int *err) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int pair = blockIdx.x;
+    const int layer = blockIdx.y >> 1;
+    uint4 *c = (blockIdx.y & 1) ? v_cache_layers[layer] : k_cache_layers[layer];
+    if (!usable(c)) {
+        if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) pk::set_error(err, PK_DEVERR_POINTER);
+        return;
+    }
+    const int64_t src = pairs[2 * pair];
+    const int64_t dst = pairs[2 * pair + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) pk::set_error(err, PK_DEVERR_PAIR);
+        return;
+    }
+    const uint4 *s = c + src * block_vecs;
+    uint4 *d = c + dst * block_vecs;
+    const int64_t lo = static_cast<int64_t>(blockIdx.z) * kCopyVecsPerCta;
+    const int64_t hi = min(lo + kCopyVecsPerCta, block_vecs);
+    uint4 buf[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t e = lo + u * kThreads + threadIdx.x;
+        if (e < hi) buf[u] = s[e];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t e = lo + u * kThreads + threadIdx.x;
+        if (e < hi) d[e] = buf[u];
+    }
+}
+
 // grid = (num_seqs, token chunks of kGatherTokens).  Each CTA walks the table
 // of one sequence for its chunk of positions.
 constexpr int kGatherTokens = 32;
@@ -161,6 +234,60 @@ extern "C" int pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_d
     copy_blocks_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs, block_vecs,
         num_blocks, err);
+    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+namespace {
+bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+}  // namespace
+
+extern "C" int pk_reshape_and_cache_layers(const void *const *k_layers, const void *const *v_layers,
+                                           void *const *k_cache_layers, void *const *v_cache_layers,
+                                           const int64_t *slot_mapping, int num_tokens, int num_layers,
+                                           int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                           pk_stream_t stream) {
+    if (num_tokens < 0 || num_layers < 0 || num_layers > 65535 || num_blocks < 0 || num_kv_heads <= 0 ||
+        block_size <= 0)
+        return PK_ERR_SHAPE;
+    if (!supported_geometry(num_kv_heads, head_dim, block_size)) return PK_ERR_UNSUPPORTED;
+    if (num_tokens == 0 || num_layers == 0) return PK_OK;
+    if (!k_layers || !v_layers || !k_cache_layers || !v_cache_layers || !slot_mapping) return PK_ERR_NULL;
+    if (!aligned8(k_layers) || !aligned8(v_layers) || !aligned8(k_cache_layers) || !aligned8(v_cache_layers))
+        return PK_ERR_ALIGNMENT;
+    const int row_vecs = num_kv_heads * head_dim / 8;
+    const int64_t total = static_cast<int64_t>(num_tokens) * row_vecs;
+    const int64_t grid = (total + kThreads - 1) / kThreads;
+    if (grid > 0x7fffffff) return PK_ERR_SHAPE;
+    unsigned int *err = pk::error_word_ptr();
+    if (!err) return PK_ERR_NO_DEVICE;
+    reshape_and_cache_layers_kernel<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(num_layers)),
+                                      kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint4 *const *>(k_layers), reinterpret_cast<const uint4 *const *>(v_layers),
+        reinterpret_cast<uint4 *const *>(k_cache_layers), reinterpret_cast<uint4 *const *>(v_cache_layers),
+        slot_mapping, num_tokens, row_vecs, static_cast<int64_t>(num_blocks) * block_size, err);
+    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+extern "C" int pk_copy_blocks_layers(void *const *k_cache_layers, void *const *v_cache_layers,
+                                     const int64_t *src_dst_pairs, int num_pairs, int num_layers,
+                                     int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                     pk_stream_t stream) {
+    if (num_pairs < 0 || num_layers < 0 || num_layers > 32767 || num_blocks < 0 || num_kv_heads <= 0 ||
+        block_size <= 0)
+        return PK_ERR_SHAPE;
+    if (!supported_geometry(num_kv_heads, head_dim, block_size)) return PK_ERR_UNSUPPORTED;
+    if (num_pairs == 0 || num_layers == 0) return PK_OK;
+    if (!k_cache_layers || !v_cache_layers || !src_dst_pairs) return PK_ERR_NULL;
+    if (!aligned8(k_cache_layers) || !aligned8(v_cache_layers)) return PK_ERR_ALIGNMENT;
+    const int64_t block_vecs = static_cast<int64_t>(block_size) * num_kv_heads * head_dim / 8;
+    const int64_t chunks = (block_vecs + kCopyVecsPerCta - 1) / kCopyVecsPerCta;
+    if (chunks > 65535) return PK_ERR_SHAPE;
+    unsigned int *err = pk::error_word_ptr();
+    if (!err) return PK_ERR_NO_DEVICE;
+    dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(2 * num_layers), static_cast<unsigned>(chunks));
+    copy_blocks_layers_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<uint4 *const *>(k_cache_layers), reinterpret_cast<uint4 *const *>(v_cache_layers),
+        src_dst_pairs, block_vecs, num_blocks, err);
     return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 

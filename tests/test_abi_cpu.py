@@ -125,6 +125,27 @@ def test_cache_ops_host_validation(lib):
         assert lib.pk_get_device_error(ctypes.byref(code), None) == -7 and code.value == 0
 
 
+def test_multi_layer_cache_ops_host_validation(lib):
+    f = lib.pk_reshape_and_cache_layers
+    #   k_layers   v_layers   kc_layers  vc_layers  slots     T  L   Hkv D    P   B
+    assert f(_fake(), _fake(), _fake(), _fake(), _fake(), 4, 80, 8, 100, 16, 16, None) == -3
+    assert f(_fake(), _fake(), _fake(), _fake(), _fake(), 4, -1, 8, 128, 16, 16, None) == -2
+    assert f(_fake(), _fake(), _fake(), _fake(), _fake(), 4, 65536, 8, 128, 16, 16, None) == -2
+    assert f(_fake(), _fake(), _fake(), _fake(), _fake(), 4, 0, 8, 128, 16, 16, None) == 0
+    assert f(_fake(), _fake(), _fake(), _fake(), _fake(), 0, 80, 8, 128, 16, 16, None) == 0
+    assert f(_fake(), _fake(), NULL, _fake(), _fake(), 4, 80, 8, 128, 16, 16, None) == -1
+    assert f(ctypes.c_void_p(_fake().value + 4), _fake(), _fake(), _fake(), _fake(), 4, 80, 8, 128, 16, 16, None) == -6
+    g = lib.pk_copy_blocks_layers
+    #   kc_layers  vc_layers  pairs    n  L   Hkv D    P   B
+    assert g(_fake(), _fake(), _fake(), 3, 80, 8, 128, 16, 12, None) == -3
+    assert g(_fake(), _fake(), _fake(), 3, 32768, 8, 128, 16, 16, None) == -2
+    assert g(_fake(), _fake(), _fake(), 0, 80, 8, 128, 16, 16, None) == 0
+    assert g(_fake(), NULL, _fake(), 2, 80, 8, 128, 16, 16, None) == -1
+    if not torch.cuda.is_available():
+        assert f(_fake(), _fake(), _fake(), _fake(), _fake(), 4, 80, 8, 128, 16, 16, None) == -7
+        assert g(_fake(), _fake(), _fake(), 2, 80, 8, 128, 16, 16, None) == -7
+
+
 def test_binding_refuses_cpu_tensors():
     import paged_kv_cache_122_gb300 as pk
     q = torch.zeros(1, 8, 64, dtype=torch.bfloat16)
