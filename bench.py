@@ -327,6 +327,60 @@ def workload_report(name, seed, dev, steps, flush, peak):
     return rep
 
 
+def swap_report(w, t, dev, nblocks=1024, reps=5):
+    """Swap `nblocks` random blocks of the pool out to a pinned host pool and
+    back in: one pk_swap_blocks launch per direction, against one
+    cudaMemcpyAsync per block and tensor (what "many small transfers" means)."""
+    import torch
+    import paged_kv_cache_122_gb300 as pk
+    import numpy as np
+    rng = np.random.default_rng(7)
+    src = rng.choice(w.num_blocks, size=nblocks, replace=False)
+    pairs_out = torch.from_numpy(np.stack([src, np.arange(nblocks)], 1).astype(np.int64)).to(dev)
+    pairs_in = torch.from_numpy(np.stack([np.arange(nblocks), src], 1).astype(np.int64)).to(dev)
+    shape = (nblocks,) + tuple(t["k_cache"].shape[1:])
+    hk = torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = 2 * nblocks * hk[0].numel() * 2
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream); fn(); b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    kc, vc = t["k_cache"], t["v_cache"]
+    out_ms = timed(lambda: pk.swap_blocks(hk, hv, kc, vc, pairs_out))
+    in_ms = timed(lambda: pk.swap_blocks(kc, vc, hk, hv, pairs_in))
+    src_l = src.tolist()
+
+    def per_block_out():
+        for i, b in enumerate(src_l):
+            hk[i].copy_(kc[b], non_blocking=True)
+            hv[i].copy_(vc[b], non_blocking=True)
+
+    def per_block_in():
+        for i, b in enumerate(src_l):
+            kc[b].copy_(hk[i], non_blocking=True)
+            vc[b].copy_(hv[i], non_blocking=True)
+    pb_out = timed(per_block_out)
+    pb_in = timed(per_block_in)
+    assert pk.pk_get_device_error(dev) == 0
+    gb = lambda ms: round(nbytes / (ms * 1e-3) / 1e9, 1)
+    return {"blocks": nblocks, "bytes": nbytes,
+            "out_one_launch_gbs": gb(out_ms), "in_one_launch_gbs": gb(in_ms),
+            "out_per_block_copies_gbs": gb(pb_out), "in_per_block_copies_gbs": gb(pb_in),
+            "what": f"{nblocks} random blocks (K+V, {hk[0].numel() * 4} B each) device pool <-> pinned "
+                    "host pool; one pk_swap_blocks launch per direction vs one cudaMemcpyAsync per block "
+                    "and tensor (median of 5)"}
+
+
 def multi_layer_report(w, t, dev, layers, steps, workspace, out, peak):
     """One attention step of a `layers`-layer model (the Llama-3-70B batch has
     80): the copy-on-write copies and the append of every layer in one launch
@@ -490,6 +544,7 @@ def run_ours(args):
     assert pk.pk_get_device_error(dev) == 0
 
     others = {}
+    swap = swap_report(w, t, dev) if args.report_workloads and rank == 0 else None
     if args.report_workloads and rank == 0:
         peak0, _ = load_peaks()
         for name in ("l3-8b", "long", "prefix-b8", "prefix-b16", "prefix-b32", "tiny"):
@@ -576,6 +631,8 @@ def run_ours(args):
         res["other_workloads"] = others
     if multi:
         res["multi_layer"] = multi
+    if swap:
+        res["block_swap"] = swap
     if rank == 0:
         r = run_block_manager(args.workload, args.seed, 50, not args.no_cpu_baseline)
         nat = statistics.median(r["native"]) * 1e6

@@ -278,6 +278,32 @@ int pk_copy_blocks_layers(void *const *k_cache_layers, void *const *v_cache_laye
                           pk_stream_t stream);
 
 /*
+ * Move blocks between two pools in one launch: for every pair (src, dst),
+ * dst_k[dst] = src_k[src] and dst_v[dst] = src_v[src], whole blocks.  One pool
+ * is typically the device pool and the other a pool in page-locked host memory
+ * that the GPU can address (cudaHostAlloc, or a torch pin_memory tensor under
+ * unified addressing): swapping a preempted request out copies its blocks to
+ * host RAM and swapping it in copies them back ("PagedAttention from First
+ * Principles", §15 "KV-cache offloading and disaggregated serving";
+ * "PagedAttention Explained", preemption by swapping or recomputation; "How
+ * vLLM and PagedAttention Actually Work", §10 Q3).  The pages note that many
+ * small transfers use the CPU-GPU link poorly; here one kernel moves every
+ * block of the batch, each warp streaming whole 512-byte runs of block rows
+ * over the link, many CTAs keeping many reads in flight.
+ *
+ *   src_k, src_v  [src_num_blocks, block_size, num_kv_heads, head_dim] bf16
+ *   dst_k, dst_v  [dst_num_blocks, block_size, num_kv_heads, head_dim] bf16
+ *   pairs         [num_pairs, 2] int64 DEVICE array of (src block, dst block)
+ *
+ * A block id outside its pool sets PK_DEVERR_PAIR and that pair is skipped.
+ * No dst may repeat and the two pools must not overlap; otherwise the result
+ * is unspecified.  num_pairs == 0 is a no-op.  Bit-exact.
+ */
+int pk_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                   const int64_t *pairs, int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int src_num_blocks, int dst_num_blocks, pk_stream_t stream);
+
+/*
  * Gather every sequence's K/V through its block table into contiguous rows:
  * out_k[cu_seq_lens[s] + j] = k_cache[block_tables[s, j / B], j % B] for
  * j < seq_lens[s] (same for V).  This is the table walk of the attention kernel

@@ -29,6 +29,7 @@ from .paged_ref import (  # noqa: F401
     merge_partials,
     reshape_and_cache,
     copy_blocks,
+    swap_blocks,
     kv_bytes_per_token,
     kv_bytes_per_block,
     block_table_bytes,

@@ -254,6 +254,27 @@ def copy_blocks(k_cache_bits: np.ndarray, v_cache_bits: np.ndarray,
     return kc, vc
 
 
+def swap_blocks(src_k_bits: np.ndarray, src_v_bits: np.ndarray, dst_k_bits: np.ndarray,
+                dst_v_bits: np.ndarray, pairs: Sequence[Sequence[int]]):
+    """Return copies of the destination pool with ``dst[d] = src[s]`` per pair.
+
+    "PagedAttention from First Principles" §15 (KV-cache offloading): a block
+    that is swapped out is copied to host RAM and its HBM slot freed; swapping
+    in copies it back.  "PagedAttention Explained" (preemption): swapping
+    copies all of an evicted request's blocks, in both directions.  The two
+    pools may have different sizes; block contents move unchanged.
+    """
+    kd = np.array(dst_k_bits, copy=True)
+    vd = np.array(dst_v_bits, copy=True)
+    for src, dst in pairs:
+        src, dst = int(src), int(dst)
+        if not (0 <= src < src_k_bits.shape[0] and 0 <= dst < kd.shape[0]):
+            raise ValueError("block id outside its pool")
+        kd[dst] = src_k_bits[src]
+        vd[dst] = src_v_bits[src]
+    return kd, vd
+
+
 # ----------------------------------------------------------------------------
 # Byte counts
 # ----------------------------------------------------------------------------

@@ -25,7 +25,9 @@ from .api import (  # noqa: F401
     pk_reshape_and_cache,
     pk_reshape_and_cache_layers,
     pk_set_decode_path,
+    pk_swap_blocks,
     reshape_and_cache,
+    swap_blocks,
 )
 from ._native import PagedKVError, load as load_library  # noqa: F401
 from .block_manager import BlockManager  # noqa: F401

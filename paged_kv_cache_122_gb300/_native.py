@@ -38,6 +38,8 @@ SIGNATURES = {
         c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "pk_copy_blocks_layers": (c_int, [
         c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "pk_swap_blocks": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "pk_gather_kv": (c_int, [
         c_void_p, c_void_p, c_void_p, c_void_p,
         c_void_p, c_int, c_void_p, c_void_p, c_int,

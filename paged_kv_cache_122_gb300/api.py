@@ -159,6 +159,34 @@ def pk_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: 
 copy_blocks = pk_copy_blocks
 
 
+def pk_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor,
+                   pairs: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks from one pool to another (e.g. device <-> pinned host)
+    for every (src, dst) row of an int64 [n, 2] device tensor.  A pool may be a
+    CUDA tensor or a pinned CPU tensor.  See the C header."""
+    dev = pairs.device
+    if not pairs.is_cuda:
+        raise ValueError("pairs must be a CUDA tensor")
+    for name, t in (("dst_k", dst_k), ("dst_v", dst_v), ("src_k", src_k), ("src_v", src_v)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 [P, B, Hkv, D] tensor")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    _need(pairs, "pairs", torch.int64, 2, dev)
+    if pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n, 2]")
+    if src_k.shape != src_v.shape or dst_k.shape != dst_v.shape or src_k.shape[1:] != dst_k.shape[1:]:
+        raise ValueError("pool shapes disagree")
+    P_src, B, Hkv, D = src_k.shape
+    with torch.cuda.device(dev):
+        st = load().pk_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(src_k), _ptr(src_v), _ptr(pairs),
+                                   pairs.shape[0], Hkv, D, B, P_src, dst_k.shape[0], _stream(dev, stream))
+    check("pk_swap_blocks", st)
+
+
+swap_blocks = pk_swap_blocks
+
+
 class LayerPointers:
     """A device array of the data pointers of per-layer tensors (what the
     ``*_layers`` calls take).  Build it once per set of layers: it holds a

@@ -145,6 +145,38 @@ copy_blocks_layers_kernel(uint4 *const *k_cache_layers, uint4 *const *v_cache_la
     }
 }
 
+// grid = (pairs, 2 [K, V], chunks of one block): the block copy of
+// copy_blocks_kernel between two pools (one of them usually host memory the
+// GPU addresses over the CPU link).  Each thread keeps four 16-byte reads in
+// flight before it writes.
+__global__ void __launch_bounds__(kThreads)
+swap_blocks_kernel(uint4 *__restrict__ dst_k, uint4 *__restrict__ dst_v, const uint4 *__restrict__ src_k,
+                   const uint4 *__restrict__ src_v, const int64_t *__restrict__ pairs, int64_t block_vecs,
+                   int src_blocks, int dst_blocks, unsigned int *err) {
+    const int pair = blockIdx.x;
+    const int64_t src = pairs[2 * pair];
+    const int64_t dst = pairs[2 * pair + 1];
+    if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+        if (blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) pk::set_error(err, PK_DEVERR_PAIR);
+        return;
+    }
+    const uint4 *s = (blockIdx.y ? src_v : src_k) + src * block_vecs;
+    uint4 *d = (blockIdx.y ? dst_v : dst_k) + dst * block_vecs;
+    const int64_t lo = static_cast<int64_t>(blockIdx.z) * kCopyVecsPerCta;
+    const int64_t hi = min(lo + kCopyVecsPerCta, block_vecs);
+    uint4 buf[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t e = lo + u * kThreads + threadIdx.x;
+        if (e < hi) buf[u] = s[e];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t e = lo + u * kThreads + threadIdx.x;
+        if (e < hi) d[e] = buf[u];
+    }
+}
+
 // grid = (num_seqs, token chunks of kGatherTokens).  Each CTA walks the table
 // of one sequence for its chunk of positions.
 constexpr int kGatherTokens = 32;
@@ -288,6 +320,28 @@ extern "C" int pk_copy_blocks_layers(void *const *k_cache_layers, void *const *v
     copy_blocks_layers_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<uint4 *const *>(k_cache_layers), reinterpret_cast<uint4 *const *>(v_cache_layers),
         src_dst_pairs, block_vecs, num_blocks, err);
+    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+extern "C" int pk_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                              const int64_t *pairs, int num_pairs, int num_kv_heads, int head_dim,
+                              int block_size, int src_num_blocks, int dst_num_blocks, pk_stream_t stream) {
+    if (num_pairs < 0 || src_num_blocks < 0 || dst_num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0)
+        return PK_ERR_SHAPE;
+    if (!supported_geometry(num_kv_heads, head_dim, block_size)) return PK_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PK_OK;
+    if (!dst_k || !dst_v || !src_k || !src_v || !pairs) return PK_ERR_NULL;
+    if (!pk::aligned16(dst_k) || !pk::aligned16(dst_v) || !pk::aligned16(src_k) || !pk::aligned16(src_v))
+        return PK_ERR_ALIGNMENT;
+    const int64_t block_vecs = static_cast<int64_t>(block_size) * num_kv_heads * head_dim / 8;
+    const int64_t chunks = (block_vecs + kCopyVecsPerCta - 1) / kCopyVecsPerCta;
+    if (chunks > 65535) return PK_ERR_SHAPE;
+    unsigned int *err = pk::error_word_ptr();
+    if (!err) return PK_ERR_NO_DEVICE;
+    dim3 grid(static_cast<unsigned>(num_pairs), 2, static_cast<unsigned>(chunks));
+    swap_blocks_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(dst_k), static_cast<uint4 *>(dst_v), static_cast<const uint4 *>(src_k),
+        static_cast<const uint4 *>(src_v), pairs, block_vecs, src_num_blocks, dst_num_blocks, err);
     return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 

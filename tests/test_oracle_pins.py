@@ -461,3 +461,29 @@ def test_copy_blocks_clones_whole_blocks_only():
     assert np.array_equal(kc2[untouched], kc[untouched]) and np.array_equal(vc2[untouched], vc[untouched])
     with pytest.raises(ValueError):
         ref.copy_blocks(kc, vc, [(0, P)])
+
+
+def test_swap_blocks_within_one_pool_is_copy_blocks_and_round_trips():
+    rng = np.random.default_rng(24)
+    P, H, B, Hkv, D = 10, 6, 4, 2, 8
+    kd = rng.integers(0, 65536, (P, B, Hkv, D), dtype=np.uint16)
+    vd = rng.integers(0, 65536, (P, B, Hkv, D), dtype=np.uint16)
+    kh = rng.integers(0, 65536, (H, B, Hkv, D), dtype=np.uint16)
+    vh = rng.integers(0, 65536, (H, B, Hkv, D), dtype=np.uint16)
+    # Inside one pool the swap is exactly the copy-on-write block copy.
+    pairs = [(1, 7), (4, 8)]
+    a = ref.swap_blocks(kd, vd, kd, vd, pairs)
+    b = ref.copy_blocks(kd, vd, pairs)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # Out to the host pool and back into other device blocks: the blocks come back unchanged.
+    out = [(2, 0), (5, 3), (9, 5)]
+    kh2, vh2 = ref.swap_blocks(kd, vd, kh, vh, out)
+    back = [(d, s) for s, d in out]
+    kd2, vd2 = ref.swap_blocks(kh2, vh2, np.zeros_like(kd), np.zeros_like(vd), back)
+    for s, _ in out:
+        assert np.array_equal(kd2[s], kd[s]) and np.array_equal(vd2[s], vd[s])
+    # Host blocks not named keep their bits.
+    keep = [b for b in range(H) if b not in {d for _, d in out}]
+    assert np.array_equal(kh2[keep], kh[keep]) and np.array_equal(vh2[keep], vh[keep])
+    with pytest.raises(ValueError):
+        ref.swap_blocks(kd, vd, kh, vh, [(0, H)])
