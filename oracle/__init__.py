@@ -25,6 +25,7 @@ from .paged_ref import (  # noqa: F401
     gather_sequence,
     softmax_attention,
     paged_decode_attention,
+    paged_multi_query_attention,
     partial_attention,
     merge_partials,
     reshape_and_cache,

@@ -165,6 +165,51 @@ def paged_decode_attention(q_bits: np.ndarray, k_cache_bits: np.ndarray,
     return out
 
 
+def paged_multi_query_attention(q_bits: np.ndarray, k_cache_bits: np.ndarray,
+                                v_cache_bits: np.ndarray, block_tables: np.ndarray,
+                                seq_lens: Sequence[int], cu_q_lens: Sequence[int], scale: float,
+                                block_size: int, seqs: Iterable[int] | None = None) -> np.ndarray:
+    """Several new query tokens per sequence over the paged cache, causal
+    among them; ``out [total_q, H, D]`` float64.
+
+    "PagedAttention from First Principles" §12 (chunked prefill: a chunk of a
+    prompt is processed over the cache in one pass) and §14 (speculative
+    decoding: the verifier checks several appended tokens in one forward
+    pass over the paged cache).  Sequence ``s`` owns query rows
+    ``cu_q_lens[s] .. cu_q_lens[s+1]-1``: its ``q_s`` newest tokens, already
+    appended, so its context has ``L = seq_lens[s]`` tokens and query ``r``
+    sits at position ``L - q_s + r``.  Causal reading (the plainest one the
+    pages support: a token never sees tokens after it): query ``r`` attends
+    keys ``0 .. L - q_s + r``.  Everything else is the decode definition.
+    """
+    Tq, H, D = q_bits.shape
+    Hkv = k_cache_bits.shape[2]
+    if H % Hkv:
+        raise ValueError("num_heads must be a multiple of num_kv_heads")
+    G = H // Hkv
+    N = len(seq_lens)
+    if len(cu_q_lens) != N + 1 or cu_q_lens[0] != 0 or cu_q_lens[N] != Tq:
+        raise ValueError("cu_q_lens must be [0, ..., total_q] with one entry per sequence plus one")
+    out = np.zeros((Tq, H, D), dtype=np.float64)
+    for s in (range(N) if seqs is None else seqs):
+        L = int(seq_lens[s])
+        q0, q1 = int(cu_q_lens[s]), int(cu_q_lens[s + 1])
+        qs = q1 - q0
+        if qs < 0 or qs > L:
+            raise ValueError("a sequence has more queries than context tokens")
+        if qs == 0:
+            continue
+        for kvh in range(Hkv):
+            K = bf16_bits_to_f64(gather_sequence(k_cache_bits, block_tables[s], L, block_size, kvh))
+            V = bf16_bits_to_f64(gather_sequence(v_cache_bits, block_tables[s], L, block_size, kvh))
+            for r in range(qs):
+                last = L - qs + r            # the query's own position
+                q = bf16_bits_to_f64(q_bits[q0 + r, kvh * G:(kvh + 1) * G, :])
+                o, _ = softmax_attention(q, K[:last + 1], V[:last + 1], scale)
+                out[q0 + r, kvh * G:(kvh + 1) * G, :] = o
+    return out
+
+
 def partial_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
     """Attention restricted to a contiguous token range: ``(lse [G], o [G, D])``.
 

@@ -487,3 +487,79 @@ def test_swap_blocks_within_one_pool_is_copy_blocks_and_round_trips():
     assert np.array_equal(kh2[keep], kh[keep]) and np.array_equal(vh2[keep], vh[keep])
     with pytest.raises(ValueError):
         ref.swap_blocks(kd, vd, kh, vh, [(0, H)])
+
+
+# ---------------------------------------------------------------------------
+# Multi-query (causal) paged attention
+# ---------------------------------------------------------------------------
+
+def _mq_case(seed, lens, qlens, H=4, Hkv=2, D=8, B=4, extra=3):
+    rng = np.random.default_rng(seed)
+    nb = [ref.num_logical_blocks(L, B) for L in lens]
+    P = sum(nb) + extra
+    perm = rng.permutation(P)
+    bt = np.full((len(lens), max(nb)), -1, dtype=np.int32)
+    k = 0
+    for s, n in enumerate(nb):
+        bt[s, :n] = perm[k:k + n]
+        k += n
+    kc = ref_bits(rng, (P, B, Hkv, D))
+    vc = ref_bits(rng, (P, B, Hkv, D))
+    cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int64)
+    q = ref_bits(rng, (int(cu[-1]), H, D))
+    return q, kc, vc, bt, cu, B
+
+
+def ref_bits(rng, shape):
+    # bf16 bit patterns of N(0, 1) draws (round to nearest even), like the workloads.
+    x = rng.standard_normal(shape).astype(np.float32).view(np.uint32)
+    return ((x + 0x7FFF + ((x >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_multi_query_with_one_query_is_decode():
+    lens = [1, 9, 23]
+    q, kc, vc, bt, cu, B = _mq_case(30, lens, [1, 1, 1])
+    a = ref.paged_multi_query_attention(q, kc, vc, bt, lens, cu, 0.35, B)
+    b = ref.paged_decode_attention(q, kc, vc, bt, lens, 0.35, B)
+    assert np.array_equal(a, b)
+
+
+def test_multi_query_full_prefill_matches_brute_force_causal_attention():
+    # Every token of the sequence is a query: masked attention written out
+    # with explicit loops and math.fsum, on the contiguous gather.
+    L, H, Hkv, D = 7, 4, 2, 8
+    q, kc, vc, bt, cu, B = _mq_case(31, [L], [L], H=H, Hkv=Hkv, D=D)
+    got = ref.paged_multi_query_attention(q, kc, vc, bt, [L], cu, 0.4, B)
+    G = H // Hkv
+    for h in range(H):
+        K = ref.bf16_bits_to_f64(ref.gather_sequence(kc, bt[0], L, B, h // G))
+        V = ref.bf16_bits_to_f64(ref.gather_sequence(vc, bt[0], L, B, h // G))
+        for i in range(L):
+            qi = ref.bf16_bits_to_f64(q[i, h])
+            z = [0.4 * math.fsum(qi[d] * K[j, d] for d in range(D)) if j <= i else -math.inf for j in range(L)]
+            m = max(z)
+            w = [math.exp(x - m) if x != -math.inf else 0.0 for x in z]
+            den = math.fsum(w)
+            want = [math.fsum(w[j] * V[j, d] for j in range(L)) / den for d in range(D)]
+            assert np.allclose(got[i, h], want, rtol=0, atol=1e-12)
+
+
+def test_multi_query_is_causal_and_equals_truncated_decode():
+    lens, qlens = [12, 5], [4, 5]
+    q, kc, vc, bt, cu, B = _mq_case(32, lens, qlens)
+    out = ref.paged_multi_query_attention(q, kc, vc, bt, lens, cu, 0.3, B)
+    # Query r of sequence s equals decode over the first L - q_s + r + 1 tokens.
+    for s, (L, qs) in enumerate(zip(lens, qlens)):
+        for r in range(qs):
+            n = L - qs + r + 1
+            one = ref.paged_decode_attention(q[cu[s] + r][None], kc, vc, bt[s:s + 1], [n], 0.3, B)
+            assert np.array_equal(out[cu[s] + r], one[0])
+    # Changing a later token's K/V leaves earlier queries unchanged.
+    pos = lens[0] - 1                                   # the last token of sequence 0
+    blk, off = bt[0, pos // B], pos % B
+    kc2 = kc.copy(); kc2[blk, off] ^= 0x0100
+    out2 = ref.paged_multi_query_attention(q, kc2, vc, bt, lens, cu, 0.3, B)
+    assert np.array_equal(out2[:cu[1] - 1], out[:cu[1] - 1])
+    assert not np.array_equal(out2[cu[1] - 1], out[cu[1] - 1])
+    with pytest.raises(ValueError):
+        ref.paged_multi_query_attention(q, kc, vc, bt, [3, 5], cu, 0.3, B)   # 4 queries, 3 tokens
