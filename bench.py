@@ -381,6 +381,35 @@ def swap_report(w, t, dev, nblocks=1024, reps=5):
                     "and tensor (median of 5)"}
 
 
+def multi_query_report(w, t, dev, flush, peak, q_per_seq=2, steps=20):
+    """Speculative-verification shape: q_per_seq newest tokens of every
+    sequence of the batch as causal queries over the paged cache (one MMA
+    column per query token and query head: G * q <= 16)."""
+    import torch
+    import paged_kv_cache_122_gb300 as pk
+    from paged_kv_cache_122_gb300 import metrics as M
+    N = w.num_seqs
+    cu = torch.arange(N + 1, dtype=torch.int32, device=dev) * q_per_seq
+    g = torch.Generator(device=dev).manual_seed(99)
+    q = torch.randn(N * q_per_seq, w.num_heads, w.head_dim, generator=g, device=dev, dtype=torch.bfloat16)
+    out = torch.empty_like(q)
+
+    def fn():
+        pk.paged_attention_multi_query(q, cu, q_per_seq, t["k_cache"], t["v_cache"], t["block_tables"],
+                                       t["seq_lens"], w.scale, out=out, max_seq_len=w.max_seq_len)
+    for _ in range(3):
+        fn()
+    ms = time_decode(fn, steps, flush, torch.cuda.current_stream(dev))
+    assert pk.pk_get_device_error(dev) == 0
+    ub = M.useful_bytes(w)
+    nbytes = ub["kv"] + q_per_seq * ub["q_o"]
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"q_per_seq": q_per_seq, "ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "query_tokens_per_s_per_layer": round(N * q_per_seq / (ms * 1e-3), 1),
+            "what": f"{N} sequences x {q_per_seq} newest tokens as causal queries (G={w.group}), "
+                    "paged_attention_multi_query, L2 flushed between calls"}
+
+
 def multi_layer_report(w, t, dev, layers, steps, workspace, out, peak):
     """One attention step of a `layers`-layer model (the Llama-3-70B batch has
     80): the copy-on-write copies and the append of every layer in one launch
@@ -545,6 +574,9 @@ def run_ours(args):
 
     others = {}
     swap = swap_report(w, t, dev) if args.report_workloads and rank == 0 else None
+    mqr = None
+    if args.report_workloads and rank == 0 and w.group * 2 <= 16:
+        mqr = multi_query_report(w, t, dev, flush, load_peaks()[0])
     if args.report_workloads and rank == 0:
         peak0, _ = load_peaks()
         for name in ("l3-8b", "long", "prefix-b8", "prefix-b16", "prefix-b32", "tiny"):
@@ -633,6 +665,8 @@ def run_ours(args):
         res["multi_layer"] = multi
     if swap:
         res["block_swap"] = swap
+    if mqr:
+        res["multi_query"] = mqr
     if rank == 0:
         r = run_block_manager(args.workload, args.seed, 50, not args.no_cpu_baseline)
         nat = statistics.median(r["native"]) * 1e6

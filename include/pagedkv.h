@@ -185,6 +185,37 @@ int pk_paged_attention_decode_noalloc(void *out, int out_dtype, const void *q,
                                       int head_dim, int num_blocks, int block_size,
                                       float scale, pk_stream_t stream);
 
+/*
+ * Attention of SEVERAL new tokens per sequence over the paged cache, causal
+ * among them: chunked prefill of a prompt ("PagedAttention from First
+ * Principles", §12) and speculative-decoding verification, where the
+ * verifier checks a few appended tokens in one pass (§14).  Sequence s owns
+ * query rows cu_q_lens[s] .. cu_q_lens[s+1]-1: its q_s newest tokens, whose
+ * K/V are already in the cache, so with L = seq_lens[s] query r sits at
+ * position L - q_s + r and attends positions 0 .. L - q_s + r.  With one
+ * query per sequence this is pk_paged_attention_decode.
+ *
+ *   out        [total_q, num_heads, head_dim], bf16 or fp32
+ *   q          [total_q, num_heads, head_dim] bf16
+ *   cu_q_lens  [num_seqs + 1] int32 DEVICE array, cu_q_lens[0] = 0,
+ *              non-decreasing, cu_q_lens[num_seqs] = total_q
+ *   max_q_len  host-side bound of cu_q_lens[s+1] - cu_q_lens[s]
+ *   everything else as for pk_paged_attention_decode (same workspace size).
+ *
+ * Tensor cores, one MMA column per (query token, query head of the group):
+ * supported while G * q <= 16 with q = max_q_len rounded up to a power of
+ * two (e.g. G = 8: 2 tokens; G = 4: 4; G = 1: 16); otherwise
+ * PK_ERR_UNSUPPORTED.  A sequence with more queries than tokens sets
+ * PK_DEVERR_SEQ_LEN (its rows are then unspecified).
+ */
+int pk_paged_attention_multi_query(void *out, int out_dtype, const void *q, int total_q,
+                                   const int32_t *cu_q_lens, int max_q_len, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables,
+                                   int max_blocks_per_seq, const int32_t *seq_lens, int max_seq_len,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                   int num_blocks, int block_size, float scale, void *workspace,
+                                   size_t workspace_bytes, pk_stream_t stream);
+
 /* Kernel family of pk_paged_attention_decode, process-wide. */
 enum pk_decode_path {
     PK_PATH_AUTO = 0,                    /* tensor cores (per-head tiles) when G >= 4,

@@ -16,6 +16,8 @@ from .api import (  # noqa: F401
     LayerPointers,
     copy_blocks,
     paged_attention_decode,
+    paged_attention_multi_query,
+    pk_paged_attention_multi_query,
     pk_copy_blocks,
     pk_copy_blocks_layers,
     pk_decode_workspace_bytes,

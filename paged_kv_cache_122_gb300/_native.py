@@ -28,6 +28,14 @@ SIGNATURES = {
     "pk_paged_attention_decode_noalloc": (c_int, [
         c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
         c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p]),
+    "pk_paged_attention_multi_query": (c_int, [
+        c_void_p, c_int, c_void_p, c_int,      # out, out_dtype, q, total_q
+        c_void_p, c_int,                       # cu_q_lens, max_q_len
+        c_void_p, c_void_p, c_void_p, c_int,   # k_cache, v_cache, block_tables, max_blocks_per_seq
+        c_void_p, c_int,                       # seq_lens, max_seq_len
+        c_int, c_int, c_int, c_int,            # num_seqs, num_heads, num_kv_heads, head_dim
+        c_int, c_int, c_float,                 # num_blocks, block_size, scale
+        c_void_p, c_size_t, c_void_p]),        # workspace, workspace_bytes, stream
     "pk_reshape_and_cache": (c_int, [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
         c_int, c_int, c_int, c_int, c_int, c_void_p]),

@@ -114,6 +114,51 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                      block_size, max_seq_len, workspace, stream)
 
 
+def paged_attention_multi_query(q: torch.Tensor, cu_q_lens: torch.Tensor, max_q_len: int,
+                                k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                seq_lens: torch.Tensor, scale: float, *, out_dtype=torch.bfloat16,
+                                max_seq_len: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal attention of several new tokens per sequence (rows cu_q_lens[s] ..
+    cu_q_lens[s+1]-1 of q, the sequence's newest tokens) over the paged cache;
+    returns [total_q, H, D].  See the C header."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 3)
+    _need(cu_q_lens, "cu_q_lens", torch.int32, 1, dev)
+    _need(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    Tq, H, D = q.shape
+    P, B, Hkv, Dk = k_cache.shape
+    N, MB = block_tables.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or Dk != D:
+        raise ValueError("k_cache / v_cache / q shapes disagree")
+    if seq_lens.shape[0] != N or cu_q_lens.shape[0] != N + 1:
+        raise ValueError("seq_lens / cu_q_lens do not match the block tables' batch")
+    if out is None:
+        out = torch.empty((Tq, H, D), dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, 3, dev)
+    if tuple(out.shape) != (Tq, H, D) or out.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out must be bf16 or fp32 [total_q, H, D]")
+    if max_seq_len is None:
+        max_seq_len = MB * B
+    ws_bytes = pk_decode_workspace_bytes(N, H, Hkv, D, max_seq_len)
+    if workspace is None:
+        workspace = workspace_for(dev, ws_bytes, stream)
+    with torch.cuda.device(dev):
+        st = load().pk_paged_attention_multi_query(
+            _ptr(out), _native.PK_FP32 if out.dtype == torch.float32 else _native.PK_BF16, _ptr(q), Tq,
+            _ptr(cu_q_lens), int(max_q_len), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), MB,
+            _ptr(seq_lens), int(max_seq_len), N, H, Hkv, D, P, B, float(scale), _ptr(workspace),
+            0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(dev, stream))
+    check("pk_paged_attention_multi_query", st)
+    return out
+
+
+pk_paged_attention_multi_query = paged_attention_multi_query
+
+
 def pk_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                          slot_mapping: torch.Tensor, stream=None) -> None:
     """Write new tokens' K/V ([T, Hkv, D] bf16) to their int64 slots.  See the C header."""

@@ -32,6 +32,14 @@ struct DecodeParams {
     void *tc_slots;
     // Head-batched path: tag of this call for the merge tickets (never 0).
     uint32_t epoch;
+    // Multi-query attention (tensor-core path): q is [total_q, H, D] and
+    // sequence s owns query rows cu_q_lens[s] .. cu_q_lens[s+1]-1, its newest
+    // tokens, causal among themselves; q_len is the padded number of query
+    // tokens per sequence the kernel packs into the MMA columns.  NULL / 1
+    // for single-token decode.
+    const int32_t *cu_q_lens;
+    int q_len;
+    int total_q;       // rows of q (multi-query)
     unsigned int *err;
 };
 
@@ -44,6 +52,9 @@ inline size_t workspace_floats(int num_seqs, int num_heads, int head_dim, int np
 
 // Tensor-core path (tcgen05): main kernel + merge of cut segments.
 cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream);
+// Multi-query attention on the tensor-core path (p.cu_q_lens set, p.q_len a
+// power of two with G * q_len <= 16).
+cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t stream);
 // Workspace bytes the tensor-core path needs (independent of the sizes).
 size_t tc_workspace_bytes();
 // Bytes of one cut-segment slot of the tensor-core path (two per CTA).

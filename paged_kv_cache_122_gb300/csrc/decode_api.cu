@@ -128,3 +128,66 @@ extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q
     if (pk::launch_decode_merge(p, st) != cudaSuccess) return PK_ERR_CUDA;
     return PK_OK;
 }
+
+extern "C" int pk_paged_attention_multi_query(void *out, int out_dtype, const void *q, int total_q,
+                                              const int32_t *cu_q_lens, int max_q_len, const void *k_cache,
+                                              const void *v_cache, const int32_t *block_tables,
+                                              int max_blocks_per_seq, const int32_t *seq_lens, int max_seq_len,
+                                              int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                              int num_blocks, int block_size, float scale, void *workspace,
+                                              size_t workspace_bytes, pk_stream_t stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
+        max_seq_len < 0 || block_size <= 0 || total_q < 0 || max_q_len < 0)
+        return PK_ERR_SHAPE;
+    if (num_heads % num_kv_heads) return PK_ERR_SHAPE;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+        return PK_ERR_SHAPE;
+    if (out_dtype != PK_BF16 && out_dtype != PK_FP32) return PK_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PK_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PK_ERR_UNSUPPORTED;
+    const int G = num_heads / num_kv_heads;
+    if (!group_supported(G)) return PK_ERR_UNSUPPORTED;
+    // Query tokens per sequence are padded to a power of two; the MMA packs
+    // G of them per KV head into at most 16 columns.
+    int ql = 1;
+    while (ql < max_q_len) ql <<= 1;
+    if (G * ql > 16) return PK_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PK_ERR_SHAPE;
+    if (num_seqs > 65535) return PK_ERR_SHAPE;
+    if (num_seqs == 0 || total_q == 0) return PK_OK;
+    if (!out || !q || !cu_q_lens || !seq_lens || (max_seq_len > 0 && (!k_cache || !v_cache || !block_tables)))
+        return PK_ERR_NULL;
+    if (!pk::aligned16(out) || !pk::aligned16(q) || !pk::aligned16(k_cache) || !pk::aligned16(v_cache))
+        return PK_ERR_ALIGNMENT;
+
+    pk::DecodeParams p{};
+    p.out = out;
+    p.out_fp32 = out_dtype == PK_FP32;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k_cache = static_cast<const uint16_t *>(k_cache);
+    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_seq_len = max_seq_len;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.scale_log2 = scale * pk::kLog2e;
+    p.cu_q_lens = cu_q_lens;
+    p.q_len = ql;
+    p.total_q = total_q;
+    if (max_seq_len > 128) {
+        if (!workspace || workspace_bytes < pk::tc_workspace_bytes()) return PK_ERR_WORKSPACE;
+        if (!pk::aligned16(workspace)) return PK_ERR_ALIGNMENT;
+        p.tc_slots = workspace;
+    }
+    p.err = pk::error_word_ptr();
+    if (!p.err) return PK_ERR_NO_DEVICE;
+    if (max_seq_len == 0) return PK_OK;   // every sequence is empty: no query can exist
+    return pk::launch_multi_query_tensor_core(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PK_OK : PK_ERR_CUDA;
+}

@@ -93,6 +93,7 @@ struct Misc {
     int never;
     uint32_t mask[kStages][4];
     int4 meta[kStages];            // (sequence, KV head, tile, tiles in segment) of a stage's tile
+    int4 qmeta[kStages];           // (first query row, query tokens, first query position, 0) of it
     float red[4][kNPad];          // per-warp maxima when the reference max moves
     float lsum[4][kNPad];
 };
@@ -154,12 +155,12 @@ __device__ __forceinline__ void store_out(const DecodeParams &p, size_t idx, flo
     else static_cast<uint16_t *>(p.out)[idx] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
 }
 
-template <int D, int G>
+template <int D, int NC, bool MQ>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(G >= 1 && G <= kNPad, "group");
+    static_assert(NC >= 1 && NC <= kNPad, "group");
     constexpr int NCH = D / 64;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -174,6 +175,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int c = blockIdx.x, C = gridDim.x;
     const int N = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads, B = p.block_size;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * B);
+    const int Gq = H / Hkv, lgG = __ffs(Gq) - 1;     // query heads per KV head (a power of two)
+    constexpr bool mq = MQ;                           // several query tokens per sequence
     Slot *slots = static_cast<Slot *>(p.tc_slots);
 
     if (threadIdx.x == 0) {
@@ -240,7 +243,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     // Empty sequences: zeros, written by CTA s % C.
     for (int s = c; s < N; s += C) {
-        if (clamp_len(p, s, cap) != 0) continue;
+        const int L = clamp_len(p, s, cap);
+        if (mq) {
+            // A sequence has at most L query tokens (they are its newest tokens).
+            const int r0 = p.cu_q_lens[s], r1 = p.cu_q_lens[s + 1];
+            if (r1 < r0 || r1 - r0 > L) set_error(p.err, PK_DEVERR_SEQ_LEN);
+            if (L != 0) continue;
+            for (int64_t i = threadIdx.x; i < static_cast<int64_t>(max(r1 - r0, 0)) * H * D; i += kThreads)
+                store_out(p, static_cast<size_t>(r0) * H * D + i, 0.f);
+            continue;
+        }
+        if (L != 0) continue;
         for (int i = threadIdx.x; i < H * D; i += kThreads) store_out(p, static_cast<size_t>(s) * H * D + i, 0.f);
     }
     tc_fence_before();
@@ -288,6 +301,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             }
             const int tok0 = w.t * kTile;
             const int vlen = min(kTile, w.L - tok0);
+            // The sequence's query rows: its newest qn tokens (one for decode).
+            int qrow0 = w.s, qn = 1;
+            if constexpr (MQ) {
+                qrow0 = p.cu_q_lens[w.s];
+                qn = p.cu_q_lens[w.s + 1] - qrow0;
+            }
+            constexpr uint32_t q_bytes = (MQ ? NC : kNPad) * 128u * NCH;
             const int pages = (vlen + B - 1) / B;
             int phys = -1;
             bool ok = false;
@@ -317,15 +337,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 misc->mask[st][2] = m2;
                 misc->mask[st][3] = m3;
                 misc->meta[st] = make_int4(w.s, w.h, w.t, w.nt);
-                mbar_arrive_expect_tx(full, nok * B * 128u * NCH + (q_resident ? 0u : kNPad * 128u * NCH));
+                if constexpr (MQ) misc->qmeta[st] = make_int4(qrow0, qn, w.L - qn, 0);
+                mbar_arrive_expect_tx(full, nok * B * 128u * NCH + (q_resident ? 0u : q_bytes));
                 mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
             }
             __syncwarp();
             // K (and Q) first: the scores can start while V is still landing.
             if (lane == 0 && !q_resident) {
 #pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_2d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, ch * 64, w.s * H + w.h * G);
+                for (int ch = 0; ch < NCH; ++ch) {
+                    if constexpr (MQ)   // box (64, G heads, q_len tokens): column r * G + g
+                        tma_load_3d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, ch * 64, w.h * Gq, qrow0);
+                    else      // box (64, 16 rows) of the [N * H, D] queries
+                        tma_load_2d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, ch * 64, w.s * H + w.h * Gq);
+                }
             }
             if (ok) {
 #pragma unroll
@@ -435,12 +460,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        float m_ref[G], l_run[G], m_prev[G], l_prev[G];
+        float m_ref[NC], l_run[NC], m_prev[NC], l_prev[NC];
 #pragma unroll
-        for (int g = 0; g < G; ++g) m_ref[g] = l_run[g] = m_prev[g] = l_prev[g] = 0.f;
+        for (int g = 0; g < NC; ++g) m_ref[g] = l_run[g] = m_prev[g] = l_prev[g] = 0.f;
         int seg = -1, seg_t0 = 0, seg_i0 = 0;
         bool pending = false;            // a finished segment awaits its read-out
-        int pend_seg = 0, pend_s = 0, pend_h = 0, pend_i = 0, pend_t0 = 0, pend_i0 = 0;
+        int pend_seg = 0, pend_s = 0, pend_h = 0, pend_i = 0, pend_t0 = 0, pend_i0 = 0, pend_q0 = 0, pend_qn = 1;
         bool pend_complete = false, pend_cut_end = false;
         auto finalize = [&]() -> bool {
             // P.V of the segment's last tile (pend_i) complete.
@@ -454,32 +479,41 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&misc->o_free[pend_seg & 1]));
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < NC; ++g) {
                 const float v = warp_sum(l_prev[g]);
                 if (lane == 0) misc->lsum[quad][g] = v;
             }
             named_bar_sync(1, 128);
-            float l[G];
+            float l[NC];
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+            for (int g = 0; g < NC; ++g)
                 l[g] = misc->lsum[0][g] + misc->lsum[1][g] + misc->lsum[2][g] + misc->lsum[3][g];
             if (pend_complete) {
                 if (row < D) {
 #pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        store_out(p, (static_cast<size_t>(pend_s) * H + pend_h * G + g) * D + row,
-                                  l[g] > 0.f ? ov[g] / l[g] : 0.f);
+                    for (int g = 0; g < NC; ++g) {
+                        if constexpr (MQ) {
+                            // Column g: query token g / G (padded columns past the
+                            // sequence's queries are not written), head g % G.
+                            if ((g >> lgG) >= pend_qn) continue;
+                            store_out(p, (static_cast<size_t>(pend_q0 + (g >> lgG)) * H + pend_h * Gq + (g & (Gq - 1))) * D + row,
+                                      l[g] > 0.f ? ov[g] / l[g] : 0.f);
+                        } else {
+                            store_out(p, (static_cast<size_t>(pend_s) * H + pend_h * NC + g) * D + row,
+                                      l[g] > 0.f ? ov[g] / l[g] : 0.f);
+                        }
+                    }
                 }
             } else {
                 const int slot_idx = pend_i0 == 0 ? 0 : 1;
                 Slot *sl = slots + 2 * c + slot_idx;
                 if (row < D) {
 #pragma unroll
-                    for (int g = 0; g < G; ++g) sl->o[g * D + row] = ov[g];
+                    for (int g = 0; g < NC; ++g) sl->o[g * D + row] = ov[g];
                 }
                 if (row == 0) {
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int g = 0; g < NC; ++g) {
                         sl->m[g] = m_prev[g];
                         sl->l[g] = l[g];
                     }
@@ -504,6 +538,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 break;
             }
             const int4 mt = misc->meta[st];   // (s, h, t, nt), written with the stage
+            int4 qm = make_int4(mt.x, 1, 0, 0);
+            if constexpr (MQ) qm = misc->qmeta[st];  // (first query row, query tokens, first query position)
             const bool seg_first = (i == 0) || (mt.z == 0);
             const bool seg_last = (i == n_tiles - 1) || (mt.z == mt.w - 1);
             if (seg_first) {
@@ -511,7 +547,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 seg_t0 = mt.z;
                 seg_i0 = i;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < NC; ++g) {
                     m_ref[g] = -INFINITY;
                     l_run[g] = 0.f;
                 }
@@ -520,24 +556,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             float sv[16];
             tmem_ld16(lane_addr + kTmemS + sb * kNPad, sv);
             const bool valid = (misc->mask[st][row >> 5] >> (row & 31)) & 1u;
-            float s2[G];
+            float s2[NC];
             bool need = false;
+            const int jpos = mt.z * kTile + row;          // this row's token position
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                s2[g] = valid ? sv[g] * p.scale_log2 : -INFINITY;
+            for (int g = 0; g < NC; ++g) {
+                // Multi-query: column g is query token g / G, which sees positions <= its own.
+                const bool vg = valid && (!mq || jpos <= qm.z + (g >> lgG));
+                s2[g] = vg ? sv[g] * p.scale_log2 : -INFINITY;
                 need |= s2[g] > m_ref[g] + kRescaleLog2;
             }
             if (named_bar_or(1, 128, need)) {
                 // Rare: move the reference to the running max.
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < NC; ++g) {
                     const float mx = warp_max(s2[g]);
                     if (lane == 0) misc->red[quad][g] = mx;
                 }
                 named_bar_sync(1, 128);
-                float a[G];
+                float a[NC];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < NC; ++g) {
                     const float t = fmaxf(fmaxf(misc->red[0][g], misc->red[1][g]),
                                           fmaxf(misc->red[2][g], misc->red[3][g]));
                     const float mn = fmaxf(m_ref[g], t);
@@ -560,11 +599,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     float lo[8], hi[8];
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
-                        lo[g] = g < G ? ov[g] * a[g < G ? g : 0] : ov[g];
-                        hi[g] = 8 + g < G ? ov[8 + g] * a[8 + g < G ? 8 + g : 0] : ov[8 + g];
+                        lo[g] = g < NC ? ov[g] * a[g < NC ? g : 0] : ov[g];
+                        hi[g] = 8 + g < NC ? ov[8 + g] * a[8 + g < NC ? 8 + g : 0] : ov[8 + g];
                     }
                     tmem_st8(oaddr, lo);
-                    if (G > 8) tmem_st8(oaddr + 8, hi);
+                    if (NC > 8) tmem_st8(oaddr + 8, hi);
                 }
                 // red[] is rewritten only in a later rare path, after the next vote.
             }
@@ -572,13 +611,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
             for (int g = 0; g < kNPad; ++g) pr[g] = 0.f;
 #pragma unroll
-            for (int g = 0; g < G; ++g) pr[g] = valid ? fast_exp2(s2[g] - m_ref[g]) : 0.f;
+            for (int g = 0; g < NC; ++g) {
+                if constexpr (MQ) pr[g] = s2[g] != -INFINITY ? fast_exp2(s2[g] - m_ref[g]) : 0.f;
+                else pr[g] = valid ? fast_exp2(s2[g] - m_ref[g]) : 0.f;
+            }
             uint32_t packed[kNPad / 2];
 #pragma unroll
             for (int gp = 0; gp < kNPad / 2; ++gp) packed[gp] = pack_bf16x2(pr[2 * gp], pr[2 * gp + 1]);
             // The denominator sums the bf16 weights the MMA actually applies.
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+            for (int g = 0; g < NC; ++g)
                 l_run[g] += (g & 1) ? bf16_hi(packed[g >> 1]) : bf16_lo(packed[g >> 1]);
             // P buffer sb is free once P.V of tile i-2 is done.
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[sb]), ((i >> 1) & 1) ^ 1, &misc->never,
@@ -623,6 +665,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 pending = true;
                 pend_seg = seg;
                 pend_s = mt.x;
+                pend_q0 = qm.x;
+                pend_qn = qm.y;
                 pend_h = mt.y;
                 pend_i = i;
                 pend_t0 = seg_t0;
@@ -630,7 +674,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 pend_complete = seg_t0 == 0 && mt.z == mt.w - 1;
                 pend_cut_end = mt.z == mt.w - 1;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < NC; ++g) {
                     m_prev[g] = m_ref[g];
                     l_prev[g] = l_run[g];
                 }
@@ -653,7 +697,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
 // One CTA per main-kernel CTA c: if c's first segment was cut at its start
 // and ends in c, combine the parts of that segment from every CTA it spans.
-template <int D, int G>
+template <int D, int NC>
 __global__ void __launch_bounds__(128)
 decode_tc_merge_kernel(const DecodeParams p, int C) {
     // Launched as a programmatic dependent of the decode grid: wait for it
@@ -670,9 +714,9 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
     const int flag = mine->flag;
     const int s = mine->s, h = mine->h;
     const int64_t start = mine->start_tile, T = mine->total_tiles;
-    float mm[G], ml[G], mo[G], am[G], al[G], ao[G], bm[G], bl[G], bo[G];
+    float mm[NC], ml[NC], mo[NC], am[NC], al[NC], ao[NC], bm[NC], bl[NC], bo[NC];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < NC; ++g) {
         mm[g] = mine->m[g];
         ml[g] = mine->l[g];
         mo[g] = mine->o[g * D + d];
@@ -686,12 +730,12 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
     if (flag != 1 || threadIdx.x >= D) return;
     int ca = static_cast<int>(start * C / T);
     while (ca + 1 < C && range_begin(ca + 1, T, C) <= start) ++ca;
-    float num[G], den[G];
+    float num[NC], den[NC];
     if (ca == c - 1) {
         // Two parts: CTA c - 1 (slot 0 if the segment is its first, else 1) and this CTA.
         const bool first_of_prev = range_begin(c - 1, T, C) >= start;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < NC; ++g) {
             const float pm = first_of_prev ? am[g] : bm[g];
             const float pl = first_of_prev ? al[g] : bl[g];
             const float po = first_of_prev ? ao[g] : bo[g];
@@ -704,32 +748,38 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
         // Contributors are the CTAs from ca to c with a non-empty range (when
         // the grid has more CTAs than tiles, some ranges are empty and hold
         // no slot).
-        float M[G];
+        float M[NC];
 #pragma unroll
-        for (int g = 0; g < G; ++g) M[g] = -INFINITY;
+        for (int g = 0; g < NC; ++g) M[g] = -INFINITY;
         for (int cc = ca; cc <= c; ++cc) {
             if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
             const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
 #pragma unroll
-            for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], sl->m[g]);
+            for (int g = 0; g < NC; ++g) M[g] = fmaxf(M[g], sl->m[g]);
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g) num[g] = den[g] = 0.f;
+        for (int g = 0; g < NC; ++g) num[g] = den[g] = 0.f;
         for (int cc = ca; cc <= c; ++cc) {
             if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
             const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < NC; ++g) {
                 const float a = rescale(sl->m[g], M[g]);
                 den[g] = fmaf(a, sl->l[g], den[g]);
                 num[g] = fmaf(a, sl->o[g * D + d], num[g]);
             }
         }
     }
+    // Column g: query token g / G of the sequence, head g % G (as in the decode kernel).
+    const int Gq = p.num_heads / p.num_kv_heads, lgG = __ffs(Gq) - 1;
+    const int q0row = p.cu_q_lens ? p.cu_q_lens[s] : s;
+    const int qn = p.cu_q_lens ? p.cu_q_lens[s + 1] - q0row : 1;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-        store_out(p, (static_cast<size_t>(s) * p.num_heads + h * G + g) * D + d,
+    for (int g = 0; g < NC; ++g) {
+        if ((g >> lgG) >= qn) continue;
+        store_out(p, (static_cast<size_t>(q0row + (g >> lgG)) * p.num_heads + h * Gq + (g & (Gq - 1))) * D + d,
                   den[g] > 0.f ? num[g] / den[g] : 0.f);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -766,6 +816,20 @@ bool encode_cache_map(CUtensorMap *m, const void *base, const DecodeParams &p) {
 bool encode_q_map(CUtensorMap *m, const DecodeParams &p) {
     auto enc = get_encoder();
     if (!enc) return false;
+    if (p.cu_q_lens) {
+        // [total_q, H, D] queries; box (64 elements, G heads, q_len tokens):
+        // MMA column r * G + g = query token r, head g of the group.
+        const int G = p.num_heads / p.num_kv_heads;
+        cuuint64_t dims3[3] = {static_cast<cuuint64_t>(p.head_dim), static_cast<cuuint64_t>(p.num_heads),
+                               static_cast<cuuint64_t>(p.total_q > 0 ? p.total_q : 1)};
+        cuuint64_t strides3[2] = {static_cast<cuuint64_t>(p.head_dim) * 2,
+                                  static_cast<cuuint64_t>(p.head_dim) * p.num_heads * 2};
+        cuuint32_t box3[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(p.q_len)};
+        cuuint32_t estr3[3] = {1, 1, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(p.q), dims3, strides3, box3,
+                   estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.head_dim),
                           static_cast<cuuint64_t>(p.num_seqs) * p.num_heads};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.head_dim) * 2};
@@ -776,13 +840,16 @@ bool encode_q_map(CUtensorMap *m, const DecodeParams &p) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G>
+template <int D, int NC>
 cudaError_t launch_dg(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const DecodeParams &p,
                       int C, cudaStream_t stream) {
     static bool attr_set = false;   // per instantiation; setting it twice is harmless
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+        cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, NC, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_tc_kernel<D, NC, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -796,18 +863,20 @@ cudaError_t launch_dg(const CUtensorMap &mk, const CUtensorMap &mv, const CUtens
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, G>, mk, mv, mq, p);
+    cudaError_t e = p.cu_q_lens ? cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NC, true>, mk, mv, mq, p)
+                                : cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NC, false>, mk, mv, mq, p);
     if (e != cudaSuccess) return e;
     if (!p.tc_slots) return cudaSuccess;   // no sequence longer than one tile: nothing is cut
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, decode_tc_merge_kernel<D, G>, p, C);
+    return cudaLaunchKernelEx(&cfg, decode_tc_merge_kernel<D, NC>, p, C);
 }
 
 template <int D>
 cudaError_t launch_d(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const DecodeParams &p,
                      int C, cudaStream_t stream) {
-    switch (p.num_heads / p.num_kv_heads) {
+    // MMA columns: the group's query heads times the query tokens per sequence.
+    switch ((p.num_heads / p.num_kv_heads) * (p.cu_q_lens ? p.q_len : 1)) {
         case 1: return launch_dg<D, 1>(mk, mv, mq, p, C, stream);
         case 2: return launch_dg<D, 2>(mk, mv, mq, p, C, stream);
         case 4: return launch_dg<D, 4>(mk, mv, mq, p, C, stream);
@@ -836,6 +905,13 @@ cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream
 namespace pk {
 
 size_t tc_slot_bytes() { return sizeof(Slot); }
+
+cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t stream) {
+    const int G = p.num_heads / p.num_kv_heads;
+    if (!p.cu_q_lens || p.q_len < 1 || (p.q_len & (p.q_len - 1)) || G * p.q_len > kNPad)
+        return cudaErrorInvalidValue;
+    return launch_decode_tensor_core(p, stream);
+}
 
 cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas) {
     CUtensorMap mk, mv, mq;

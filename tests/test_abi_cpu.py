@@ -146,6 +146,21 @@ def test_multi_layer_cache_ops_host_validation(lib):
         assert g(_fake(), _fake(), _fake(), 2, 80, 8, 128, 16, 16, None) == -7
 
 
+def test_multi_query_host_validation(lib):
+    f = lib.pk_paged_attention_multi_query
+    def call(tq=8, cu="fake", mq=2, h=16, hkv=2, d=128, msl=64, nseq=4):
+        return f(_fake(), 0, _fake(), tq, _fake() if cu == "fake" else cu, mq, _fake(), _fake(), _fake(), 4,
+                 _fake(), msl, nseq, h, hkv, d, 16, 16, 0.1, _fake(), 1 << 30, None)
+    assert call(mq=3) == -3                   # 8 heads x 4 (padded) query tokens > 16 columns
+    assert call(h=8, hkv=8, mq=17) == -3      # G = 1: at most 16 query tokens
+    assert call(d=96) == -3
+    assert call(tq=0) == 0 and call(nseq=0) == 0
+    assert call(cu=NULL) == -1
+    assert call(tq=-1) == -2
+    if not torch.cuda.is_available():
+        assert call() == -7
+
+
 def test_binding_refuses_cpu_tensors():
     import paged_kv_cache_122_gb300 as pk
     q = torch.zeros(1, 8, 64, dtype=torch.bfloat16)

@@ -1,0 +1,79 @@
+"""Multi-query paged attention (several newest tokens per sequence, causal
+among them) on the tensor cores against the float64 oracle, and one query
+per sequence against the decode call bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_122_gb300 as pk
+from paged_kv_cache_122_gb300 import workloads as W
+from paritylib import assert_close, host_bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _case(seed, lens, qlens, G, Hkv, D, B):
+    w = W.custom(seed, lens, G * Hkv, Hkv, D, B)
+    t = W.make_tensors(w, DEV)
+    cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    g = torch.Generator().manual_seed(seed + 100)
+    q = torch.randn(int(cu[-1]), G * Hkv, D, generator=g).to(torch.bfloat16).to(DEV)
+    return w, t, q, cu
+
+
+def _run(w, t, q, cu, qmax, out_dtype=torch.float32):
+    return pk.paged_attention_multi_query(q, torch.from_numpy(cu).to(DEV), qmax, t["k_cache"], t["v_cache"],
+                                          t["block_tables"], t["seq_lens"], w.scale, out_dtype=out_dtype,
+                                          max_seq_len=w.max_seq_len)
+
+
+def _ref(w, t, q, cu):
+    return oracle.paged_multi_query_attention(host_bits(q), host_bits(t["k_cache"]), host_bits(t["v_cache"]),
+                                              w.block_tables, w.seq_lens, cu.tolist(), w.scale, w.block_size)
+
+
+@pytest.mark.parametrize("G,qmax", [(8, 2), (4, 4), (2, 8), (1, 16), (16, 1), (4, 3), (1, 5)])
+@pytest.mark.parametrize("D,B", [(128, 16), (64, 8), (128, 32)])
+def test_multi_query_matches_oracle(G, qmax, D, B):
+    Hkv = 2
+    rng = np.random.default_rng(G * 100 + qmax + D + B)
+    lens = [1, 2, 17, 128, 129, 300, 700, 1500]
+    qlens = [min(L, int(rng.integers(1, qmax + 1))) for L in lens]
+    qlens[-1] = qmax                                      # the widest case occurs
+    w, t, q, cu = _case(7, lens, qlens, G, Hkv, D, B)
+    out = _run(w, t, q, cu, qmax)
+    assert_close(out.cpu().numpy(), _ref(w, t, q, cu), False, f"G={G} q={qmax} D={D} B={B}")
+    assert pk.pk_get_device_error() == 0
+
+
+def test_multi_query_bf16_out_and_full_prefill_of_short_sequences():
+    # q = L: every token of the sequence is a query (a whole prompt chunk).
+    lens = [1, 3, 8, 16]
+    w, t, q, cu = _case(11, lens, lens, 1, 4, 128, 16)
+    out = _run(w, t, q, cu, 16, torch.bfloat16)
+    assert_close(out.float().cpu().numpy(), _ref(w, t, q, cu), True, "full prefill")
+
+
+def test_one_query_per_sequence_equals_decode_bit_for_bit():
+    lens = [5, 130, 900, 2049]
+    G, Hkv = 8, 2
+    w, t, q, cu = _case(13, lens, [1] * len(lens), G, Hkv, 128, 16)
+    prev = pk.pk_set_decode_path("tensor_core")
+    try:
+        dec = pk.paged_attention_decode(q, t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"],
+                                        w.scale, w.block_size, out_dtype=torch.float32,
+                                        max_seq_len=w.max_seq_len)
+    finally:
+        pk.pk_set_decode_path(prev)
+    mq = _run(w, t, q, cu, 1)
+    assert torch.equal(dec, mq)
+
+
+def test_unsupported_width_is_refused():
+    lens = [40]
+    w, t, q, cu = _case(3, lens, [3], 8, 2, 128, 16)
+    with pytest.raises(pk.PagedKVError) as e:
+        _run(w, t, q, cu, 3)                               # 8 heads x 4 (padded) tokens > 16 columns
+    assert e.value.status == -3
