@@ -410,6 +410,39 @@ def multi_query_report(w, t, dev, flush, peak, q_per_seq=2, steps=20):
                     "paged_attention_multi_query, L2 flushed between calls"}
 
 
+def prefill_report(dev, flush, steps=10, N=16, prior=4096, chunk=512):
+    """Chunked prefill: `chunk` new prompt tokens per sequence (causal among
+    themselves) over `prior` earlier tokens, Llama-3-70B heads (64 q / 8 kv,
+    d 128, block 16); FLOPs count only the visible (query, key) pairs."""
+    import torch
+    import paged_kv_cache_122_gb300 as pk
+    from paged_kv_cache_122_gb300 import workloads as W
+    L = prior + chunk
+    w = W.custom(3, [L] * N, 64, 8, 128, 16)
+    t = W.make_tensors(w, dev)
+    cu = torch.arange(N + 1, dtype=torch.int32, device=dev) * chunk
+    g = torch.Generator(device=dev).manual_seed(5)
+    q = torch.randn(N * chunk, 64, 128, generator=g, device=dev, dtype=torch.bfloat16)
+    out = torch.empty_like(q)
+
+    def fn():
+        pk.paged_attention_multi_query(q, cu, chunk, t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"],
+                                       w.scale, out=out, max_seq_len=w.max_seq_len)
+    for _ in range(3):
+        fn()
+    ms = time_decode(fn, steps, flush, torch.cuda.current_stream(dev))
+    assert pk.pk_get_device_error(dev) == 0
+    visible = N * sum(prior + r + 1 for r in range(chunk))          # (query token, key) pairs
+    flops = 4.0 * 128 * 64 * visible                                 # QK^T and PV, every query head
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    peak = float(peaks.get("bf16_tflops") or 0) or None
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak, 4) if peak else None,
+            "prompt_tokens_per_s_per_layer": round(N * chunk / (ms * 1e-3), 1),
+            "what": f"{N} sequences x {chunk}-token prompt chunk over {prior} earlier tokens, 64 q / 8 kv heads, "
+                    "d 128, block 16; paged_attention_multi_query (128 query rows per CTA); causal FLOPs"}
+
+
 def multi_layer_report(w, t, dev, layers, steps, workspace, out, peak):
     """One attention step of a `layers`-layer model (the Llama-3-70B batch has
     80): the copy-on-write copies and the append of every layer in one launch
@@ -605,6 +638,7 @@ def run_ours(args):
     mqr = None
     if args.report_workloads and rank == 0 and w.group * 2 <= 16:
         mqr = multi_query_report(w, t, dev, flush, load_peaks()[0])
+    pfr = prefill_report(dev, flush) if args.report_workloads and rank == 0 else None
     if args.report_workloads and rank == 0:
         peak0, _ = load_peaks()
         for name in ("l3-8b", "long", "prefix-b8", "prefix-b16", "prefix-b32", "tiny"):
@@ -697,6 +731,8 @@ def run_ours(args):
         res["block_swap"] = swap
     if mqr:
         res["multi_query"] = mqr
+    if pfr:
+        res["chunked_prefill"] = pfr
     if rank == 0:
         r = run_block_manager(args.workload, args.seed, 50, not args.no_cpu_baseline)
         nat = statistics.median(r["native"]) * 1e6

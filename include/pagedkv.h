@@ -202,11 +202,13 @@ int pk_paged_attention_decode_noalloc(void *out, int out_dtype, const void *q,
  *   max_q_len  host-side bound of cu_q_lens[s+1] - cu_q_lens[s]
  *   everything else as for pk_paged_attention_decode (same workspace size).
  *
- * Tensor cores, one MMA column per (query token, query head of the group):
- * supported while G * q <= 16 with q = max_q_len rounded up to a power of
- * two (e.g. G = 8: 2 tokens; G = 4: 4; G = 1: 16); otherwise
- * PK_ERR_UNSUPPORTED.  A sequence with more queries than tokens sets
- * PK_DEVERR_SEQ_LEN (its rows are then unspecified).
+ * Tensor cores.  Narrow blocks (G * q <= 16 with q = max_q_len rounded up
+ * to a power of two: e.g. G = 8, 2 tokens; speculative verification) use
+ * one MMA column per (query token, query head) in the decode kernel; wider
+ * blocks (prompt chunks) use a kernel with 128 query rows (128 / G tokens x
+ * G heads) per CTA over the sequence's key tiles; the workspace is then not
+ * used.  A sequence with more queries than tokens sets PK_DEVERR_SEQ_LEN
+ * (its rows are then unspecified).
  */
 int pk_paged_attention_multi_query(void *out, int out_dtype, const void *q, int total_q,
                                    const int32_t *cu_q_lens, int max_q_len, const void *k_cache,

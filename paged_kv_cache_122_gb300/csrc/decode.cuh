@@ -55,6 +55,9 @@ cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream
 // Multi-query attention on the tensor-core path (p.cu_q_lens set, p.q_len a
 // power of two with G * q_len <= 16).
 cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t stream);
+// Multi-query attention for wide query blocks (chunked prefill): 128 query
+// rows (128 / G tokens x G heads) per CTA over the paged keys; no workspace.
+cudaError_t launch_prefill_tensor_core(const DecodeParams &p, int max_q_len, cudaStream_t stream);
 // Workspace bytes the tensor-core path needs (independent of the sizes).
 size_t tc_workspace_bytes();
 // Bytes of one cut-segment slot of the tensor-core path (two per CTA).

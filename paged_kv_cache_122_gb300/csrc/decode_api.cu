@@ -147,11 +147,12 @@ extern "C" int pk_paged_attention_multi_query(void *out, int out_dtype, const vo
     if (block_size != 8 && block_size != 16 && block_size != 32) return PK_ERR_UNSUPPORTED;
     const int G = num_heads / num_kv_heads;
     if (!group_supported(G)) return PK_ERR_UNSUPPORTED;
-    // Query tokens per sequence are padded to a power of two; the MMA packs
-    // G of them per KV head into at most 16 columns.
+    // Narrow query blocks (G x q <= 16, q padded to a power of two) run on the
+    // decode kernel's 16 query columns; wider ones on the prefill kernel,
+    // 128 query rows per CTA.
     int ql = 1;
     while (ql < max_q_len) ql <<= 1;
-    if (G * ql > 16) return PK_ERR_UNSUPPORTED;
+    const bool narrow = G * ql <= 16;
     if (!std::isfinite(scale)) return PK_ERR_SHAPE;
     if (num_seqs > 65535) return PK_ERR_SHAPE;
     if (num_seqs == 0 || total_q == 0) return PK_OK;
@@ -180,7 +181,7 @@ extern "C" int pk_paged_attention_multi_query(void *out, int out_dtype, const vo
     p.cu_q_lens = cu_q_lens;
     p.q_len = ql;
     p.total_q = total_q;
-    if (max_seq_len > 128) {
+    if (narrow && max_seq_len > 128) {
         if (!workspace || workspace_bytes < pk::tc_workspace_bytes()) return PK_ERR_WORKSPACE;
         if (!pk::aligned16(workspace)) return PK_ERR_ALIGNMENT;
         p.tc_slots = workspace;
@@ -188,6 +189,9 @@ extern "C" int pk_paged_attention_multi_query(void *out, int out_dtype, const vo
     p.err = pk::error_word_ptr();
     if (!p.err) return PK_ERR_NO_DEVICE;
     if (max_seq_len == 0) return PK_OK;   // every sequence is empty: no query can exist
+    if (!narrow)
+        return pk::launch_prefill_tensor_core(p, max_q_len, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? PK_OK : PK_ERR_CUDA;
     return pk::launch_multi_query_tensor_core(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PK_OK : PK_ERR_CUDA;
 }

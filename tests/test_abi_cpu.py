@@ -151,8 +151,7 @@ def test_multi_query_host_validation(lib):
     def call(tq=8, cu="fake", mq=2, h=16, hkv=2, d=128, msl=64, nseq=4):
         return f(_fake(), 0, _fake(), tq, _fake() if cu == "fake" else cu, mq, _fake(), _fake(), _fake(), 4,
                  _fake(), msl, nseq, h, hkv, d, 16, 16, 0.1, _fake(), 1 << 30, None)
-    assert call(mq=3) == -3                   # 8 heads x 4 (padded) query tokens > 16 columns
-    assert call(h=8, hkv=8, mq=17) == -3      # G = 1: at most 16 query tokens
+    assert call(d=64, hkv=3) == -2            # 16 heads do not split into 3 KV heads
     assert call(d=96) == -3
     assert call(tq=0) == 0 and call(nseq=0) == 0
     assert call(cu=NULL) == -1

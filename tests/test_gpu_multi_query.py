@@ -71,9 +71,31 @@ def test_one_query_per_sequence_equals_decode_bit_for_bit():
     assert torch.equal(dec, mq)
 
 
-def test_unsupported_width_is_refused():
-    lens = [40]
-    w, t, q, cu = _case(3, lens, [3], 8, 2, 128, 16)
-    with pytest.raises(pk.PagedKVError) as e:
-        _run(w, t, q, cu, 3)                               # 8 heads x 4 (padded) tokens > 16 columns
-    assert e.value.status == -3
+@pytest.mark.parametrize("G,qmax", [(8, 3), (8, 64), (4, 100), (1, 300), (16, 40), (2, 129)])
+@pytest.mark.parametrize("D,B", [(128, 16), (64, 32), (128, 8)])
+def test_wide_query_blocks_match_oracle(G, qmax, D, B):
+    # Prompt chunks: 128 / G query tokens x G heads per CTA over the key tiles.
+    Hkv = 2
+    rng = np.random.default_rng(G * 1000 + qmax + D + B)
+    lens = [1, 5, 130, 300, 700, 1111]
+    qlens = [min(L, int(rng.integers(1, qmax + 1))) for L in lens]
+    qlens[-1] = qmax
+    qlens[2] = 130                                       # a whole prompt as one chunk
+    qmax = max(qlens)
+    w, t, q, cu = _case(17, lens, qlens, G, Hkv, D, B)
+    out = _run(w, t, q, cu, qmax)
+    assert_close(out.cpu().numpy(), _ref(w, t, q, cu), False, f"wide G={G} q={qmax} D={D} B={B}")
+    assert pk.pk_get_device_error() == 0
+
+
+def test_wide_block_bf16_out_with_garbage_table_padding():
+    lens = [40, 513, 1024]
+    w = W.custom(19, lens, 16, 2, 128, 16, pad="garbage")
+    t = W.make_tensors(w, DEV)
+    qlens = [40, 200, 512]
+    cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(int(cu[-1]), 16, 128, generator=g).to(torch.bfloat16).to(DEV)
+    out = _run(w, t, q, cu, 512, torch.bfloat16)
+    assert_close(out.float().cpu().numpy(), _ref(w, t, q, cu), True, "wide bf16")
+    assert pk.pk_get_device_error() == 0
