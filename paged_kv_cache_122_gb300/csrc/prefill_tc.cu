@@ -33,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 namespace pk {
 namespace {
@@ -293,18 +294,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             for (int c = 0; c < 4; ++c) msk[c] = misc->mask[st][c];
             const int kbase = i * kKeys;
             const uint32_t sbase = lane_addr + kTmemS + (i & 1) * kKeys;
-            // Pass 1: the row's maximum over this tile's visible keys.
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float sv[32];
-                tmem_ld<32>(sbase + c * 32, sv);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const bool vis = ((msk[c] >> k) & 1u) && kbase + c * 32 + k <= qp;
-                    if (vis) tmax = fmaxf(tmax, sv[k] * p.scale_log2);
-                }
-            }
             // P and O are free once P.V of the previous tile is done.
             if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done), (i - 1) & 1, &misc->never,
                                                             kWaitLimitNs))) {
@@ -312,9 +301,62 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 break;
             }
             tc_fence_after();
+            // One pass over S: the row's tile max and, against the current
+            // reference max, p = 2^(s - m_ref) as bf16 in the MMA's swizzled
+            // K-major layout plus their sum.  Tiles every key of which this
+            // row sees skip the masks.
+            // (Warp-uniform: the TMEM loads inside are warp-collective.)
+            const bool easy = __all_sync(0xffffffffu, kbase + kKeys - 1 <= qp &&
+                                                          (msk[0] & msk[1] & msk[2] & msk[3]) == 0xffffffffu);
+            float l_tile = 0.f;
+            auto run = [&](auto easy_tag, bool emit) -> float {
+                constexpr bool kEasy = decltype(easy_tag)::value;
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float sv[32];
+                    tmem_ld<32>(sbase + c * 32, sv);
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        float pr[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float x = sv[k + e] * p.scale_log2;
+                            bool vis = true;
+                            if constexpr (!kEasy)
+                                vis = ((msk[c] >> (k + e)) & 1u) && kbase + c * 32 + k + e <= qp;
+                            if (vis) tmax = fmaxf(tmax, x);
+                            pr[e] = vis ? fast_exp2(x - m_ref) : 0.f;
+                        }
+                        packed[k / 2] = pack_bf16x2(pr[0], pr[1]);
+                        // The denominator sums the bf16 weights the MMA actually applies.
+                        l_tile += bf16_lo(packed[k / 2]) + bf16_hi(packed[k / 2]);
+                    }
+                    if (emit) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int unit = c * 4 + u;                   // 8 keys = 16 bytes
+                            uint8_t *dst = p_ptr + (unit >> 3) * kChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4);
+                            *reinterpret_cast<uint4 *>(dst) =
+                                make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+                        }
+                    }
+                }
+                return tmax;
+            };
+            auto pass = [&](bool emit) -> float {
+                l_tile = 0.f;
+                return easy ? run(std::true_type{}, emit) : run(std::false_type{}, emit);
+            };
+            // Against no reference yet (first tile) only the max is useful.
+            const bool first = __any_sync(0xffffffffu, m_ref == -INFINITY);
+            const float tmax = pass(!first);
             const bool need = tmax > m_ref + kRescaleLog2;
             if (__any_sync(0xffffffffu, need)) {
-                // Move this row's reference max; rescale its O and denominator.
+                // Move this row's reference max, rescale its O and denominator,
+                // and redo the tile against the new reference (rare after the
+                // first tile).
                 const float mn = need ? tmax : m_ref;
                 const float a = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - mn);
                 if (i > 0) {
@@ -329,33 +371,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 l_run *= a;
                 m_ref = mn;
+                pass(true);
+            } else if (first) {
+                pass(true);
             }
-            // Pass 2: p = 2^(s - m_ref) as bf16 in the MMA's swizzled K-major layout.
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float sv[32];
-                tmem_ld<32>(sbase + c * 32, sv);
-                uint32_t packed[16];
-#pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    float pr[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const bool vis = ((msk[c] >> (k + e)) & 1u) && kbase + c * 32 + k + e <= qp;
-                        pr[e] = vis ? fast_exp2(sv[k + e] * p.scale_log2 - m_ref) : 0.f;
-                    }
-                    packed[k / 2] = pack_bf16x2(pr[0], pr[1]);
-                    // The denominator sums the bf16 weights the MMA actually applies.
-                    l_run += bf16_lo(packed[k / 2]) + bf16_hi(packed[k / 2]);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int unit = c * 4 + u;                   // 8 keys = 16 bytes
-                    uint8_t *dst = p_ptr + (unit >> 3) * kChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(dst) =
-                        make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
-                }
-            }
+            l_run += l_tile;
             // V rows of keys outside the sequence or behind a bad table entry
             // may hold stale or non-finite bits; the MMA multiplies them by 0,
             // so zero them (thread <-> key row) once V has landed.
