@@ -20,12 +20,15 @@
 //             heads x 128/G tokens per 64-column chunk), then per key tile
 //             each page's K rows and V rows of this KV head into a 2-stage
 //             ring (K and V complete separate barriers);
-//   warp 1    MMA issuer (one thread): S of tile i, then P.V of tile i-1;
+//   warp 1    MMA issuer (one thread): S of tile i, then P.V of tile i-1
+//             with P read from tensor memory;
 //   warps 2-5 softmax, thread <-> query row: row max against a reference
 //             max that moves only when exceeded by more than 2^8 (then the
 //             row's O and denominator are rescaled), p = 2^(s - m_ref) with
-//             the causal and validity masks, bf16 P rows written in the MMA's
-//             128-byte-swizzled K-major layout, and at the end O / l stored.
+//             the causal and validity masks, bf16 P rows stored into TMEM
+//             (double-buffered, so the softmax of tile i never waits for the
+//             P.V of tile i-1 unless its O must be rescaled), and at the end
+//             O / l stored.
 #include "decode.cuh"
 #include "sm100.cuh"
 
@@ -42,17 +45,17 @@ using namespace sm100;
 
 constexpr int kRows = 128;                      // query rows per CTA = MMA M
 constexpr int kKeys = 128;                      // keys per tile = MMA N of S
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr uint32_t kChunk = 128 * 128;          // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kKOff = 0;
 constexpr uint32_t kVOff = 2 * kChunk;
 constexpr uint32_t kStageBytes = 4 * kChunk;    // K and V of one key tile (D <= 128)
 constexpr uint32_t kQBytes = 2 * kChunk;
-constexpr uint32_t kPBytes = 2 * kChunk;        // 128 rows x 128 keys bf16
-constexpr uint32_t kTmemCols = 512;             // S x2 (128 cols each) + O (<= 128 cols)
+constexpr uint32_t kTmemCols = 512;             // S x2 (128 cols each), O (<= 128 cols), P x2 (64 cols each)
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;                // bf16 P: two keys per 32-bit column
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -63,7 +66,7 @@ struct Misc {
     uint64_t q_full;
     uint64_t s_full[2];         // S of a tile in TMEM (by tile parity)
     uint64_t p_full;            // P of a tile written (4 softmax warps)
-    uint64_t pv_done;           // P.V of a tile done (P buffer and O free)
+    uint64_t pv_done[2];        // P.V of a tile done (by tile parity): its P buffer and O free
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -71,7 +74,7 @@ struct Misc {
     uint32_t mask[kStages][4];  // valid keys of a stage's tile
 };
 
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBytes + kPBytes + sizeof(Misc);
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBytes + sizeof(Misc);
 
 __device__ __forceinline__ void store_row_out(const DecodeParams &p, size_t idx, float v) {
     if (p.out_fp32) static_cast<float *>(p.out)[idx] = v;
@@ -113,11 +116,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t *stage_ptr = smem;
     uint8_t *q_ptr = smem + kStages * kStageBytes;
-    uint8_t *p_ptr = q_ptr + kQBytes;
-    Misc *misc = reinterpret_cast<Misc *>(p_ptr + kPBytes);
+    Misc *misc = reinterpret_cast<Misc *>(q_ptr + kQBytes);
     const uint32_t stage_addr = smem_u32(stage_ptr);
     const uint32_t q_addr = smem_u32(q_ptr);
-    const uint32_t p_addr = smem_u32(p_ptr);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -129,7 +130,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         mbar_init(smem_u32(&misc->s_full[0]), 1);
         mbar_init(smem_u32(&misc->s_full[1]), 1);
         mbar_init(smem_u32(&misc->p_full), 4);
-        mbar_init(smem_u32(&misc->pv_done), 1);
+        mbar_init(smem_u32(&misc->pv_done[0]), 1);
+        mbar_init(smem_u32(&misc->pv_done[1]), 1);
         mbar_init(smem_u32(&misc->drain), 1);
         misc->abort = 0;
         misc->never = 0;
@@ -227,7 +229,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // next tile are computed while the softmax works on the current one.
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kRows, kKeys, 0, 0);   // A = Q, B = K, both K-major
-            constexpr uint32_t kIdescO = idesc_bf16(kRows, D, 0, 1);       // A = P (K-major), B = V (MN-major)
+            constexpr uint32_t kIdescO = idesc_bf16(kRows, D, 0, 1);       // A = P (TMEM), B = V (MN-major)
             bool alive = mbar_wait(smem_u32(&misc->q_full), 0, &misc->abort, kWaitLimitNs);
             auto pv = [&](int t) {
                 alive = alive && mbar_wait(smem_u32(&misc->p_full), t & 1, &misc->abort, kWaitLimitNs) &&
@@ -238,11 +240,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const uint32_t vbase = stage_addr + (t % kStages) * kStageBytes + kVOff;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t a = smem_desc(p_addr + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024, kLayoutSw128);
                     const uint64_t b = smem_desc(vbase + kk * 16 * 128, kChunk, 1024, kLayoutSw128);
-                    mma_bf16(tmem + kTmemO, a, b, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + (t & 1) * 64 + kk * 8, b, kIdescO,
+                                    (t > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(smem_u32(&misc->pv_done));
+                mma_commit(smem_u32(&misc->pv_done[t & 1]));
                 mma_commit(smem_u32(&misc->empty[t % kStages]));
             };
             for (int i = 0; i < n_tiles && alive; ++i) {
@@ -294,16 +296,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             for (int c = 0; c < 4; ++c) msk[c] = misc->mask[st][c];
             const int kbase = i * kKeys;
             const uint32_t sbase = lane_addr + kTmemS + (i & 1) * kKeys;
-            // P and O are free once P.V of the previous tile is done.
-            if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done), (i - 1) & 1, &misc->never,
-                                                            kWaitLimitNs))) {
+            // This tile's P buffer is free once P.V of tile i - 2 is done (long ago).
+            if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[i & 1]), ((i - 2) >> 1) & 1,
+                                                             &misc->never, kWaitLimitNs))) {
                 alive = false;
                 break;
             }
             tc_fence_after();
+            const uint32_t pbase = lane_addr + kTmemP + (i & 1) * 64;
             // One pass over S: the row's tile max and, against the current
-            // reference max, p = 2^(s - m_ref) as bf16 in the MMA's swizzled
-            // K-major layout plus their sum.  Tiles every key of which this
+            // reference max, p = 2^(s - m_ref) as bf16 pairs into this tile's
+            // P columns of TMEM (the P.V MMA's A operand) plus their sum.  Tiles every key of which this
             // row sees skip the masks.
             // (Warp-uniform: the TMEM loads inside are warp-collective.)
             const bool easy = __all_sync(0xffffffffu, kbase + kKeys - 1 <= qp &&
@@ -333,15 +336,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         // The denominator sums the bf16 weights the MMA actually applies.
                         l_tile += bf16_lo(packed[k / 2]) + bf16_hi(packed[k / 2]);
                     }
-                    if (emit) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int unit = c * 4 + u;                   // 8 keys = 16 bytes
-                            uint8_t *dst = p_ptr + (unit >> 3) * kChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4);
-                            *reinterpret_cast<uint4 *>(dst) =
-                                make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
-                        }
-                    }
+                    if (emit) tmem_st16(pbase + c * 16, packed);   // keys 32c .. 32c+31 of this row
                 }
                 return tmax;
             };
@@ -359,6 +354,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 // first tile).
                 const float mn = need ? tmax : m_ref;
                 const float a = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - mn);
+                // O holds tiles up to i - 1: wait for that P.V (the only wait on it).
+                if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[(i - 1) & 1]),
+                                                                ((i - 1) >> 1) & 1, &misc->never, kWaitLimitNs))) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
                 if (i > 0) {
 #pragma unroll
                     for (int c = 0; c < D / 8; ++c) {
@@ -396,12 +398,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     }
                 }
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();                 // P is in TMEM before the MMA may read it
+            fence_proxy_async_smem();       // zeroed V rows are visible to the MMA
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&misc->p_full));
         }
-        if (alive && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done), (n_tiles - 1) & 1,
+        if (alive && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[(n_tiles - 1) & 1]),
+                                                         ((n_tiles - 1) >> 1) & 1,
                                                          &misc->never, kWaitLimitNs)))
             alive = false;
         if (!alive) {

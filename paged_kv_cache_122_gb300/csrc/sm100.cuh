@@ -135,6 +135,18 @@ SM100_DEV void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (M rows = TMEM lanes,
+// K-major, two bf16 per 32-bit column) is read from tensor memory.
+SM100_DEV void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 SM100_DEV void mma_commit(uint32_t bar) {
@@ -205,6 +217,19 @@ SM100_DEV void tmem_st8(uint32_t taddr, const float (&v)[8]) {
                  : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane (32x32b);
+// completion is awaited with tmem_wait_st().
+SM100_DEV void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    __syncwarp();
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                   "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+                   "r"(v[15])
+                 : "memory");
+}
+SM100_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Named barrier over `nthreads` threads that also ORs a predicate across them.
 SM100_DEV bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
