@@ -51,7 +51,7 @@ DOMINANT_SOURCES = ["paged_kv_cache_122_gb300/csrc/decode_tc.cu", "paged_kv_cach
                     "paged_kv_cache_122_gb300/csrc/block_scan.cuh"]
 # DRAM bytes per launch of the dominant kernel from one ncu capture, and the
 # hash of its sources at that time (profiles/ holds the summary).
-RECORDED_TRAFFIC = {"sources_sha1": "52deaa7021eea1134acabb9fa370f7e6b35a7ec0", "bytes_per_launch": 1124681984, "workload": "l3-70b"}
+RECORDED_TRAFFIC = {"sources_sha1": "ff025ba528f21389863abe59ad9fea2e2c1867d1", "bytes_per_launch": 1124640512, "workload": "l3-70b"}
 
 
 def sources_sha1() -> str:
@@ -808,6 +808,9 @@ def main():
     ap.add_argument("--layers", type=int, default=1,
                     help="also time one attention step of a model with this many layers (separate caches; "
                          "multi-layer copy/append launches), e.g. 80 for Llama-3-70B")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the chunked-prefill workload (16 x 512-token chunks over 4096 earlier tokens) "
+                         "and print its report; a small case for profiling the prefill kernel")
     ap.add_argument("--cpu-seqs", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-seqs", type=int, default=32)
@@ -815,6 +818,13 @@ def main():
                     help="kernel family of paged_attention_decode (auto: tensor cores for G >= 4)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
+    if args.prefill_only:
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        print(json.dumps({"prefill": prefill_report(dev, flush, steps=args.steps)}), flush=True)
+        return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)

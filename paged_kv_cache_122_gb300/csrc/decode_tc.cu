@@ -176,6 +176,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int N = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads, B = p.block_size;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * B);
     const int Gq = H / Hkv, lgG = __ffs(Gq) - 1;     // query heads per KV head (a power of two)
+    // V of a tile in shared memory: one slot of v_page bytes per page, each
+    // [half][row][64] (B is 8, 16 or 32).
+    const uint32_t v_page = static_cast<uint32_t>(B) * 128u * NCH;
+    const uint32_t v_half = static_cast<uint32_t>(B) * 128u;        // between the two 64-element halves
+    const uint32_t v_group = B >= 16 ? 1024u : v_page;              // between groups of 8 tokens
     constexpr bool mq = MQ;                           // several query tokens per sequence
     Slot *slots = static_cast<Slot *>(p.tc_slots);
 
@@ -356,9 +361,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
                     tma_load_4d(sbase + kKOff + ch * kChunkBytes + r0 * 128, &tm_k, full, ch * 64, w.h, 0, phys);
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_4d(sbase + kVOff + ch * kChunkBytes + r0 * 128, &tm_v, vfull, ch * 64, w.h, 0, phys);
+                // V: one box per page, [half][row][64] at the page's slot.
+                tma_load_5d(sbase + kVOff + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, w.h, phys);
             }
             ++issued;
             w.next(p, cap);
@@ -384,7 +388,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const uint32_t pbase = p_addr + pb * kPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t a = smem_desc(vbase + kk * 16 * 128, kChunkBytes, 1024, kLayoutSw128);
+                    // Tokens 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
+                    const uint32_t t0 = kk * 16;
+                    const uint64_t a = smem_desc(vbase + (t0 / B) * v_page + (t0 % B) * 128, v_half, v_group,
+                                                 kLayoutSw128);
                     const uint64_t b = smem_desc(pbase + kk * 512, 256, 128, kLayoutNone);
                     mma_bf16(tmem + kTmemO + (sg & 1) * kNPad, a, b, kIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
@@ -642,7 +649,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 // masked tokens may hold stale or non-finite bits, so zero them.
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
-                    uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + ch * kChunkBytes + row * 128);
+                    uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + (row / B) * v_page +
+                                                            ch * B * 128 + (row % B) * 128);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
                 }
@@ -799,6 +807,23 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
+// V pages: one box per (page, head) holding all B rows of both 64-element
+// halves, laid out [half][row][64] in shared memory (dimensions: 64
+// elements, row, half (128 bytes apart), head, page).
+bool encode_value_map(CUtensorMap *m, const void *base, const DecodeParams &p) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    const cuuint64_t D = p.head_dim, Hkv = p.num_kv_heads, B = p.block_size;
+    const cuuint64_t P = p.num_blocks > 0 ? p.num_blocks : 1;
+    cuuint64_t dims[5] = {64, B, D / 64, Hkv, P};
+    cuuint64_t strides[4] = {Hkv * D * 2, 128, D * 2, B * Hkv * D * 2};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(B), static_cast<cuuint32_t>(D / 64), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_cache_map(CUtensorMap *m, const void *base, const DecodeParams &p) {
     auto enc = get_encoder();
     if (!enc) return false;
@@ -892,7 +917,7 @@ size_t tc_workspace_bytes() { return 2 * kMaxCtas * sizeof(Slot); }
 
 cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream) {
     CUtensorMap mk, mv, mq;
-    if (!encode_cache_map(&mk, p.k_cache, p) || !encode_cache_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
+    if (!encode_cache_map(&mk, p.k_cache, p) || !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
         return cudaErrorInvalidValue;
     int C = sm_count();
     if (C <= 0) return cudaErrorNoDevice;
@@ -916,7 +941,7 @@ cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t s
 cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas) {
     CUtensorMap mk, mv, mq;
     if (ctas <= 0 || ctas > static_cast<int>(kMaxCtas)) return cudaErrorInvalidValue;
-    if (!encode_cache_map(&mk, p.k_cache, p) || !encode_cache_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
+    if (!encode_cache_map(&mk, p.k_cache, p) || !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
         return cudaErrorInvalidValue;
     return p.head_dim == 64 ? launch_d<64>(mk, mv, mq, p, ctas, stream) : launch_d<128>(mk, mv, mq, p, ctas, stream);
 }

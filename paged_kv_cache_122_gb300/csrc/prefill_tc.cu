@@ -31,6 +31,7 @@
 //             O / l stored.
 #include "decode.cuh"
 #include "sm100.cuh"
+#include "tmem_wide.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -97,6 +98,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int h = (blockIdx.x / qblocks) % Hkv;
     const int s = blockIdx.x / qblocks / Hkv;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * B);
+    // V of a tile in shared memory: one slot of v_page bytes per page, each
+    // [half][row][64] (B is 8, 16 or 32).
+    const uint32_t v_page = static_cast<uint32_t>(B) * 128u * NCH;
+    const uint32_t v_half = static_cast<uint32_t>(B) * 128u;        // between the two 64-element halves
+    const uint32_t v_group = B >= 16 ? 1024u : v_page;              // between groups of 8 keys
     int L = p.seq_lens[s];
     const int q0 = p.cu_q_lens[s];
     const int qn = p.cu_q_lens[s + 1] - q0;
@@ -158,9 +164,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             for (int ch = 0; ch < NCH; ++ch)
                 tma_load_3d(q_addr + ch * kChunk, &tm_q, qf, ch * 64, h * G, q0 + qt0);
         }
+        // Block-table entries of a tile, one page per lane; the next tile's
+        // are fetched while the current tile's copies are issued.
+        auto fetch = [&](int t) -> int {
+            const int tok = t * kKeys;
+            const int pg = (min(kKeys, L - tok) + B - 1) / B;
+            return lane < pg ? p.block_tables[static_cast<size_t>(s) * MB + tok / B + lane] : -1;
+        };
+        int phys_next = fetch(0);
         int issued = 0;
         for (int i = 0; i < n_tiles; ++i) {
             const int st = i % kStages;
+            const int phys_raw = phys_next;
             int got = 1;
             if (lane == 0)
                 got = mbar_wait(smem_u32(&misc->empty[st]), ((i / kStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
@@ -177,7 +192,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             int phys = -1;
             bool ok = false;
             if (lane < pages) {
-                phys = p.block_tables[static_cast<size_t>(s) * MB + tok0 / B + lane];
+                phys = phys_raw;
                 ok = phys >= 0 && phys < p.num_blocks;
                 if (!ok) set_error(p.err, PK_DEVERR_BLOCK_ID);
             }
@@ -209,11 +224,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
                     tma_load_4d(sbase + kKOff + ch * kChunk + r0 * 128, &tm_k, full, ch * 64, h, 0, phys);
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_4d(sbase + kVOff + ch * kChunk + r0 * 128, &tm_v, vfull, ch * 64, h, 0, phys);
+                // V: one box per page, [half][row][64] at the page's slot.
+                tma_load_5d(sbase + kVOff + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, h, phys);
             }
             ++issued;
+            if (i + 1 < n_tiles) phys_next = fetch(i + 1);
         }
         if (misc->abort && lane == 0) {
             mbar_wait(smem_u32(&misc->q_full), 0, &misc->never, kWaitLimitNs);
@@ -240,7 +255,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const uint32_t vbase = stage_addr + (t % kStages) * kStageBytes + kVOff;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t b = smem_desc(vbase + kk * 16 * 128, kChunk, 1024, kLayoutSw128);
+                    // Keys 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
+                    const uint32_t t0 = kk * 16;
+                    const uint64_t b = smem_desc(vbase + (t0 / B) * v_page + (t0 % B) * 128, v_half, v_group,
+                                                 kLayoutSw128);
                     mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + (t & 1) * 64 + kk * 8, b, kIdescO,
                                     (t > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -296,62 +314,61 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             for (int c = 0; c < 4; ++c) msk[c] = misc->mask[st][c];
             const int kbase = i * kKeys;
             const uint32_t sbase = lane_addr + kTmemS + (i & 1) * kKeys;
+            // The row's 128 scores of this tile into registers (two loads in
+            // flight, one wait).
+            uint32_t sa[64], sb[64];
+            tmemw::ld64(sbase, sa);
+            tmemw::ld64(sbase + 64, sb);
             // This tile's P buffer is free once P.V of tile i - 2 is done (long ago).
             if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[i & 1]), ((i - 2) >> 1) & 1,
                                                              &misc->never, kWaitLimitNs))) {
                 alive = false;
                 break;
             }
+            tmemw::wait_ld(sa);
+            tmemw::wait_ld(sb);
             tc_fence_after();
             const uint32_t pbase = lane_addr + kTmemP + (i & 1) * 64;
-            // One pass over S: the row's tile max and, against the current
-            // reference max, p = 2^(s - m_ref) as bf16 pairs into this tile's
-            // P columns of TMEM (the P.V MMA's A operand) plus their sum.  Tiles every key of which this
-            // row sees skip the masks.
-            // (Warp-uniform: the TMEM loads inside are warp-collective.)
-            const bool easy = __all_sync(0xffffffffu, kbase + kKeys - 1 <= qp &&
+            auto score = [&](int k) -> float { return __uint_as_float(k < 64 ? sa[k] : sb[k - 64]); };
+            // Key k of the tile is visible to this row if its page was
+            // loaded and it is not after the row's own position.
+            const int lim = qp - kbase;
+            auto visible = [&](int k) -> bool { return ((msk[k >> 5] >> (k & 31)) & 1u) && k <= lim; };
+            // Tiles every key of which this row sees skip the masks
+            // (warp-uniform: the tensor-memory moves below are warp-collective).
+            const bool easy = __all_sync(0xffffffffu, kKeys - 1 <= lim &&
                                                           (msk[0] & msk[1] & msk[2] & msk[3]) == 0xffffffffu);
-            float l_tile = 0.f;
-            auto run = [&](auto easy_tag, bool emit) -> float {
+            const float c = p.scale_log2;
+            // The tile's row max of c * s over the visible keys, from the raw
+            // scores (c >= 0: the max, c < 0: the min; rounding is monotone,
+            // so the product of the extreme equals the extreme of the
+            // products).  Eight independent chains; a masked key is NaN,
+            // which fmaxf / fminf skip.
+            float ext[8];
+            auto gather = [&](auto easy_tag) {
                 constexpr bool kEasy = decltype(easy_tag)::value;
-                float tmax = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float sv[32];
-                    tmem_ld<32>(sbase + c * 32, sv);
-                    uint32_t packed[16];
+                for (int e = 0; e < 8; ++e) ext[e] = kEasy ? score(e) : (visible(e) ? score(e) : __int_as_float(0x7fffffff));
 #pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
-                        float pr[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const float x = sv[k + e] * p.scale_log2;
-                            bool vis = true;
-                            if constexpr (!kEasy)
-                                vis = ((msk[c] >> (k + e)) & 1u) && kbase + c * 32 + k + e <= qp;
-                            if (vis) tmax = fmaxf(tmax, x);
-                            pr[e] = vis ? fast_exp2(x - m_ref) : 0.f;
-                        }
-                        packed[k / 2] = pack_bf16x2(pr[0], pr[1]);
-                        // The denominator sums the bf16 weights the MMA actually applies.
-                        l_tile += bf16_lo(packed[k / 2]) + bf16_hi(packed[k / 2]);
-                    }
-                    if (emit) tmem_st16(pbase + c * 16, packed);   // keys 32c .. 32c+31 of this row
+                for (int k = 8; k < kKeys; ++k) {
+                    const float v = kEasy ? score(k) : (visible(k) ? score(k) : __int_as_float(0x7fffffff));
+                    ext[k & 7] = c >= 0.f ? fmaxf(ext[k & 7], v) : fminf(ext[k & 7], v);
                 }
-                return tmax;
             };
-            auto pass = [&](bool emit) -> float {
-                l_tile = 0.f;
-                return easy ? run(std::true_type{}, emit) : run(std::false_type{}, emit);
-            };
-            // Against no reference yet (first tile) only the max is useful.
-            const bool first = __any_sync(0xffffffffu, m_ref == -INFINITY);
-            const float tmax = pass(!first);
+            if (easy) gather(std::true_type{});
+            else gather(std::false_type{});
+            float e4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) e4[e] = c >= 0.f ? fmaxf(ext[e], ext[e + 4]) : fminf(ext[e], ext[e + 4]);
+            const float e2a = c >= 0.f ? fmaxf(e4[0], e4[2]) : fminf(e4[0], e4[2]);
+            const float e2b = c >= 0.f ? fmaxf(e4[1], e4[3]) : fminf(e4[1], e4[3]);
+            const float ex = c >= 0.f ? fmaxf(e2a, e2b) : fminf(e2a, e2b);
+            // No visible key (NaN): no candidate for the reference max.
+            const float tmax = ex == ex ? ex * c : -INFINITY;
             const bool need = tmax > m_ref + kRescaleLog2;
             if (__any_sync(0xffffffffu, need)) {
-                // Move this row's reference max, rescale its O and denominator,
-                // and redo the tile against the new reference (rare after the
-                // first tile).
+                // Move this row's reference max and rescale its O and
+                // denominator (rare after the first tile).
                 const float mn = need ? tmax : m_ref;
                 const float a = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - mn);
                 // O holds tiles up to i - 1: wait for that P.V (the only wait on it).
@@ -363,25 +380,52 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 tc_fence_after();
                 if (i > 0) {
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
+                    for (int cc = 0; cc < D / 8; ++cc) {
                         float ov[8];
-                        tmem_ld<8>(lane_addr + kTmemO + c * 8, ov);
+                        tmem_ld<8>(lane_addr + kTmemO + cc * 8, ov);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) ov[k] *= a;
-                        tmem_st8(lane_addr + kTmemO + c * 8, ov);
+                        tmem_st8(lane_addr + kTmemO + cc * 8, ov);
                     }
                 }
                 l_run *= a;
                 m_ref = mn;
-                pass(true);
-            } else if (first) {
-                pass(true);
             }
-            l_run += l_tile;
+            // p = 2^(c * s - m_ref) as bf16 pairs into this tile's P columns of
+            // TMEM (the P.V MMA's A operand); the denominator sums the bf16
+            // weights the MMA actually applies, in four chains.
+            const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            auto emit = [&](auto easy_tag) {
+                constexpr bool kEasy = decltype(easy_tag)::value;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const int kk = cc * 32 + k;
+                        float p0 = fast_exp2(fmaf(score(kk), c, nm));
+                        float p1 = fast_exp2(fmaf(score(kk + 1), c, nm));
+                        if constexpr (!kEasy) {
+                            p0 = visible(kk) ? p0 : 0.f;
+                            p1 = visible(kk + 1) ? p1 : 0.f;
+                        }
+                        const uint32_t w = pack_bf16x2(p0, p1);
+                        packed[k / 2] = w;
+                        ls[(k / 2) & 3] += bf16_lo(w) + bf16_hi(w);
+                    }
+                    tmem_st16(pbase + cc * 16, packed);   // keys 32cc .. 32cc+31 of this row
+                }
+            };
+            if (easy) emit(std::true_type{});
+            else emit(std::false_type{});
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // V rows of keys outside the sequence or behind a bad table entry
             // may hold stale or non-finite bits; the MMA multiplies them by 0,
             // so zero them (thread <-> key row) once V has landed.
-            const bool bad = !((msk[row >> 5] >> (row & 31)) & 1u);
+            const int wrow = row >> 5;                      // select, not an indexed load: msk stays in registers
+            const uint32_t mrow = wrow == 0 ? msk[0] : wrow == 1 ? msk[1] : wrow == 2 ? msk[2] : msk[3];
+            const bool bad = !((mrow >> (row & 31)) & 1u);
             if (__any_sync(0xffffffffu, bad)) {
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->vfull[st]), (i / kStages) & 1, &misc->never,
                                                        kWaitLimitNs))) {
@@ -391,8 +435,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (bad) {
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch) {
-                        uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + ch * kChunk +
-                                                                row * 128);
+                        uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + (row / B) * v_page +
+                                                                ch * B * 128 + (row % B) * 128);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
                     }
@@ -460,7 +504,7 @@ bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, 
             const cuuint32_t *box) {
     auto enc = encoder();
     if (!enc) return false;
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -473,11 +517,15 @@ cudaError_t launch_dg(const DecodeParams &p, int max_q_len, cudaStream_t stream)
     const cuuint64_t cdims[4] = {Dd, Hkv, B, P};
     const cuuint64_t cstr[3] = {Dd * 2, Hkv * Dd * 2, B * Hkv * Dd * 2};
     const cuuint32_t cbox[4] = {64, 1, static_cast<cuuint32_t>(B), 1};
+    // V: one box per (page, head) with all B rows of both halves, [half][row][64].
+    const cuuint64_t vdims[5] = {64, B, Dd / 64, Hkv, P};
+    const cuuint64_t vstr[4] = {Hkv * Dd * 2, 128, Dd * 2, B * Hkv * Dd * 2};
+    const cuuint32_t vbox[5] = {64, static_cast<cuuint32_t>(B), static_cast<cuuint32_t>(Dd / 64), 1, 1};
     const cuuint64_t qdims[3] = {Dd, static_cast<cuuint64_t>(p.num_heads), static_cast<cuuint64_t>(p.total_q)};
     const cuuint64_t qstr[2] = {Dd * 2, Dd * p.num_heads * 2};
     const cuuint32_t qbox[3] = {64, G, kRows / G};
     CUtensorMap mk, mv, mq;
-    if (!encode(&mk, p.k_cache, 4, cdims, cstr, cbox) || !encode(&mv, p.v_cache, 4, cdims, cstr, cbox) ||
+    if (!encode(&mk, p.k_cache, 4, cdims, cstr, cbox) || !encode(&mv, p.v_cache, 5, vdims, vstr, vbox) ||
         !encode(&mq, p.q, 3, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
