@@ -440,7 +440,7 @@ def prefill_report(dev, flush, steps=10, N=16, prior=4096, chunk=512):
     return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak, 4) if peak else None,
             "prompt_tokens_per_s_per_layer": round(N * chunk / (ms * 1e-3), 1),
             "what": f"{N} sequences x {chunk}-token prompt chunk over {prior} earlier tokens, 64 q / 8 kv heads, "
-                    "d 128, block 16; paged_attention_multi_query (128 query rows per CTA); causal FLOPs"}
+                    "d 128, block 16; paged_attention_multi_query (two 128-row query tiles per CTA); causal FLOPs"}
 
 
 def multi_layer_report(w, t, dev, layers, steps, workspace, out, peak):

@@ -6,29 +6,37 @@
 // Mathematical Formulation, Equation 4, with the causal limit).
 //
 // Orientation.  The decode kernel puts keys on the MMA's M and at most 16
-// query columns on N.  Here the queries are the dense side: a CTA owns 128
-// query rows -- 128 / G consecutive query tokens x the G query heads of one
-// KV head, row = token * G + head -- and streams the sequence's keys in
-// 128-token tiles:
+// query columns on N.  Here the queries are the dense side: a query tile is
+// 128 rows -- 128 / G consecutive query tokens x the G query heads of one
+// KV head, row = token * G + head -- and the sequence's keys stream by in
+// 128-key tiles:
 //   S[128 x 128]  = Q[128 x D] K_tile^T          (tcgen05, fp32 in TMEM)
 //   O[128 x D]   += P[128 x 128] V_tile[128 x D]  (tcgen05, fp32 in TMEM)
-// so one thread of the softmax warps owns one query row of S, P and O and
-// needs no cross-thread reduction.
+// so one softmax thread owns one query row of S, P and O and needs no
+// cross-thread reduction.
 //
-// Per CTA (192 threads):
-//   warp 0    producer: the Q block once (one TMA box of 64 elements x G
-//             heads x 128/G tokens per 64-column chunk), then per key tile
-//             each page's K rows and V rows of this KV head into a 2-stage
-//             ring (K and V complete separate barriers);
-//   warp 1    MMA issuer (one thread): S of tile i, then P.V of tile i-1
-//             with P read from tensor memory;
-//   warps 2-5 softmax, thread <-> query row: row max against a reference
-//             max that moves only when exceeded by more than 2^8 (then the
-//             row's O and denominator are rescaled), p = 2^(s - m_ref) with
-//             the causal and validity masks, bf16 P rows stored into TMEM
-//             (double-buffered, so the softmax of tile i never waits for the
-//             P.V of tile i-1 unless its O must be rescaled), and at the end
-//             O / l stored.
+// A CTA holds TWO query tiles, X = 0 and X = 1 (consecutive token blocks of
+// the same sequence and KV head), which share every K and V tile: each
+// page is fetched once per 256 query rows.  The two tiles' softmax warp
+// groups alternate with the tensor core (while one group turns its S into
+// P, the MMAs of the other tile run).  Tensor memory (512 columns) holds
+// S_0, S_1, O_0, O_1; the bf16 P of a tile is written over the first 64
+// columns of its own S (two keys per column), which the P.V MMA reads as
+// its A operand; the next S of that tile is issued after that P.V, and
+// tcgen05 MMAs of one thread execute in issue order.
+//
+// Per CTA (320 threads):
+//   warp 0     producer: both Q tiles once, then per key tile the K rows
+//              of each page (two 64-element halves) into a K ring and the
+//              V rows of each page (one box) into a V ring;
+//   warp 1     MMA issuer (one thread): per key tile i, P.V(i-1) then S(i)
+//              for tile 0, then the same for tile 1;
+//   warps 2-5  softmax of tile 0, warps 6-9 softmax of tile 1: row max
+//              against a reference max that moves only when exceeded by
+//              more than 2^8 (then the row's O and denominator are
+//              rescaled), p = 2^(s - m_ref) with the causal and validity
+//              masks, bf16 P into tensor memory, and at the end O / l
+//              written out (a TMA store of the tile when it is full).
 #include "decode.cuh"
 #include "sm100.cuh"
 #include "tmem_wide.cuh"
@@ -44,62 +52,81 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kRows = 128;                      // query rows per CTA = MMA M
+constexpr int kRows = 128;                      // query rows per tile = MMA M
 constexpr int kKeys = 128;                      // keys per tile = MMA N of S
-constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr int kMaskRing = 4;                    // tile masks in flight (producer runs <= 2 tiles ahead)
+constexpr int kThreads = 320;
 constexpr uint32_t kChunk = 128 * 128;          // 128 rows x 128 bytes (64 bf16)
-constexpr uint32_t kKOff = 0;
-constexpr uint32_t kVOff = 2 * kChunk;
-constexpr uint32_t kStageBytes = 4 * kChunk;    // K and V of one key tile (D <= 128)
-constexpr uint32_t kQBytes = 2 * kChunk;
-constexpr uint32_t kTmemCols = 512;             // S x2 (128 cols each), O (<= 128 cols), P x2 (64 cols each)
-constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 256;
-constexpr uint32_t kTmemP = 384;                // bf16 P: two keys per 32-bit column
+constexpr uint32_t kQBytes = 2 * kChunk;        // one query tile (D <= 128)
+constexpr uint32_t kKBytes = 2 * kChunk;        // K of one key tile
+constexpr uint32_t kVBytes = 2 * kChunk;        // V of one key tile
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kKOff = 2 * kQBytes;
+constexpr uint32_t kVOff = kKOff + kKStages * kKBytes;
+constexpr uint32_t kTmemCols = 512;             // S_0, S_1, O_0, O_1 (128 columns each)
+constexpr uint32_t kTmemS = 0;                  // + X * 128; P_X over its first 64 columns
+constexpr uint32_t kTmemO = 256;                // + X * 128
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 
 struct Misc {
-    uint64_t full[kStages];     // K rows of a stage landed
-    uint64_t vfull[kStages];    // V rows of a stage landed
-    uint64_t empty[kStages];    // P.V of the stage's tile done
+    uint64_t kfull[kKStages];   // K rows of a tile landed
+    uint64_t kempty[kKStages];  // both S of the tile done: K slot free
+    uint64_t vfull[kVStages];   // V rows of a tile landed
+    uint64_t vempty[kVStages];  // both P.V of the tile done: V slot free
     uint64_t q_full;
-    uint64_t s_full[2];         // S of a tile in TMEM (by tile parity)
-    uint64_t p_full;            // P of a tile written (4 softmax warps)
-    uint64_t pv_done[2];        // P.V of a tile done (by tile parity): its P buffer and O free
+    uint64_t s_full[2];         // S of query tile X in TMEM
+    uint64_t p_full[2];         // P of query tile X written (4 softmax warps)
+    uint64_t pv_done[2];        // P.V of query tile X done
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
     int never;
-    uint32_t mask[kStages][4];  // valid keys of a stage's tile
+    uint32_t mask[kMaskRing][4];  // valid keys of a key tile (by tile index mod 4)
 };
 
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBytes + sizeof(Misc);
+constexpr size_t kSmemBytes = 1024 + kVOff + kVStages * kVBytes + sizeof(Misc);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void store_row_out(const DecodeParams &p, size_t idx, float v) {
     if (p.out_fp32) static_cast<float *>(p.out)[idx] = v;
     else static_cast<uint16_t *>(p.out)[idx] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
 }
 
-// grid: one CTA per (sequence, KV head, query block of 128 / G tokens),
-// blockIdx.x = (s * Hkv + h) * qblocks + j; CTAs past a sequence's queries exit.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void group_bar(uint32_t id) {
+    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+// grid: one CTA per (sequence, KV head, pair of query tiles of 128 / G
+// tokens each), blockIdx.x = (s * Hkv + h) * qblocks + j; CTAs past a
+// sequence's queries exit.  tm_o (bf16 output only, o_tma != 0) stores
+// full query tiles.
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p, int qblocks) {
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                  const DecodeParams p, int qblocks, int o_tma) {
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(G >= 1 && G <= 16 && (G & (G - 1)) == 0, "group");
     constexpr int NCH = D / 64;
-    constexpr int QT = kRows / G;                 // query tokens per CTA
+    constexpr int QT = kRows / G;                 // query tokens per tile
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = p.num_kv_heads, H = p.num_heads, B = p.block_size;
     const int j = blockIdx.x % qblocks;
     const int h = (blockIdx.x / qblocks) % Hkv;
     const int s = blockIdx.x / qblocks / Hkv;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * B);
-    // V of a tile in shared memory: one slot of v_page bytes per page, each
-    // [half][row][64] (B is 8, 16 or 32).
+    // V of a key tile in shared memory: one slot of v_page bytes per page,
+    // each [half][row][64] (B is 8, 16 or 32).
     const uint32_t v_page = static_cast<uint32_t>(B) * 128u * NCH;
     const uint32_t v_half = static_cast<uint32_t>(B) * 128u;        // between the two 64-element halves
     const uint32_t v_group = B >= 16 ? 1024u : v_page;              // between groups of 8 keys
@@ -110,34 +137,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (j == 0 && h == 0 && threadIdx.x == 0) set_error(p.err, PK_DEVERR_SEQ_LEN);
         return;
     }
-    const int qt0 = j * QT;                       // first query token of this CTA
+    const int qt0 = j * 2 * QT;                   // first query token of tile 0
     if (qt0 >= qn) return;
-    const int qt1 = min(qn, qt0 + QT);
     const int pos0 = L - qn;                      // position of the sequence's first query
-    const int last_pos = pos0 + qt1 - 1;          // the last key any row of this CTA sees
-    const int n_tiles = last_pos / kKeys + 1;
+    // Key tiles each query tile needs (the last key it sees is that of its
+    // last token); tile 1 may be empty.
+    const int n0 = (pos0 + min(qn, qt0 + QT) - 1) / kKeys + 1;
+    const int n1 = qt0 + QT < qn ? (pos0 + min(qn, qt0 + 2 * QT) - 1) / kKeys + 1 : 0;
+    const int nT = max(n0, n1);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    uint8_t *stage_ptr = smem;
-    uint8_t *q_ptr = smem + kStages * kStageBytes;
-    Misc *misc = reinterpret_cast<Misc *>(q_ptr + kQBytes);
-    const uint32_t stage_addr = smem_u32(stage_ptr);
-    const uint32_t q_addr = smem_u32(q_ptr);
+    Misc *misc = reinterpret_cast<Misc *>(smem + kVOff + kVStages * kVBytes);
+    const uint32_t base = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&misc->full[i]), 1);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(smem_u32(&misc->kfull[i]), 1);
+            mbar_init(smem_u32(&misc->kempty[i]), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(smem_u32(&misc->vfull[i]), 1);
-            mbar_init(smem_u32(&misc->empty[i]), 1);
+            mbar_init(smem_u32(&misc->vempty[i]), 1);
         }
         mbar_init(smem_u32(&misc->q_full), 1);
-        mbar_init(smem_u32(&misc->s_full[0]), 1);
-        mbar_init(smem_u32(&misc->s_full[1]), 1);
-        mbar_init(smem_u32(&misc->p_full), 4);
-        mbar_init(smem_u32(&misc->pv_done[0]), 1);
-        mbar_init(smem_u32(&misc->pv_done[1]), 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(smem_u32(&misc->s_full[x]), 1);
+            mbar_init(smem_u32(&misc->p_full[x]), 4);
+            mbar_init(smem_u32(&misc->pv_done[x]), 1);
+        }
         mbar_init(smem_u32(&misc->drain), 1);
         misc->abort = 0;
         misc->never = 0;
@@ -159,26 +188,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             const uint32_t qf = smem_u32(&misc->q_full);
-            mbar_arrive_expect_tx(qf, kRows * 128u * NCH);
+            const int tiles = n1 > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(qf, tiles * kRows * 128u * NCH);
+            for (int x = 0; x < tiles; ++x) {
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
-                tma_load_3d(q_addr + ch * kChunk, &tm_q, qf, ch * 64, h * G, q0 + qt0);
+                for (int ch = 0; ch < NCH; ++ch)
+                    tma_load_3d(base + kQOff + x * kQBytes + ch * kChunk, &tm_q, qf, ch * 64, h * G,
+                                q0 + qt0 + x * QT);
+            }
         }
-        // Block-table entries of a tile, one page per lane; the next tile's
-        // are fetched while the current tile's copies are issued.
+        // Block-table entries of a key tile, one page per lane; the next
+        // tile's are fetched while the current tile's copies are issued.
         auto fetch = [&](int t) -> int {
             const int tok = t * kKeys;
             const int pg = (min(kKeys, L - tok) + B - 1) / B;
             return lane < pg ? p.block_tables[static_cast<size_t>(s) * MB + tok / B + lane] : -1;
         };
         int phys_next = fetch(0);
-        int issued = 0;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int st = i % kStages;
+        int kissued = 0, vissued = 0;
+        for (int i = 0; i < nT; ++i) {
+            const int kst = i % kKStages, vst = i % kVStages;
             const int phys_raw = phys_next;
             int got = 1;
             if (lane == 0)
-                got = mbar_wait(smem_u32(&misc->empty[st]), ((i / kStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
+                got = mbar_wait(smem_u32(&misc->kempty[kst]), ((i / kKStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
             if (!__shfl_sync(0xffffffffu, got, 0)) {
                 if (lane == 0) {
                     misc->abort = 1;
@@ -208,80 +241,103 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const uint32_t m2 = __reduce_or_sync(0xffffffffu, word == 2 ? bits : 0u);
             const uint32_t m3 = __reduce_or_sync(0xffffffffu, word == 3 ? bits : 0u);
             const uint32_t nok = __popc(__ballot_sync(0xffffffffu, ok));
-            const uint32_t full = smem_u32(&misc->full[st]);
-            const uint32_t vfull = smem_u32(&misc->vfull[st]);
-            const uint32_t sbase = stage_addr + st * kStageBytes;
+            const uint32_t kfull = smem_u32(&misc->kfull[kst]);
             if (lane == 0) {
-                misc->mask[st][0] = m0;
-                misc->mask[st][1] = m1;
-                misc->mask[st][2] = m2;
-                misc->mask[st][3] = m3;
-                mbar_arrive_expect_tx(full, nok * B * 128u * NCH);
-                mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
+                uint32_t *mk = misc->mask[i % kMaskRing];
+                mk[0] = m0;
+                mk[1] = m1;
+                mk[2] = m2;
+                mk[3] = m3;
+                mbar_arrive_expect_tx(kfull, nok * B * 128u * NCH);
             }
             __syncwarp();
             if (ok) {
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_4d(sbase + kKOff + ch * kChunk + r0 * 128, &tm_k, full, ch * 64, h, 0, phys);
-                // V: one box per page, [half][row][64] at the page's slot.
-                tma_load_5d(sbase + kVOff + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, h, phys);
+                    tma_load_4d(base + kKOff + kst * kKBytes + ch * kChunk + r0 * 128, &tm_k, kfull, ch * 64, h, 0,
+                                phys);
             }
-            ++issued;
-            if (i + 1 < n_tiles) phys_next = fetch(i + 1);
+            ++kissued;
+            if (lane == 0)
+                got = mbar_wait(smem_u32(&misc->vempty[vst]), ((i / kVStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
+            if (!__shfl_sync(0xffffffffu, got, 0)) {
+                if (lane == 0) {
+                    misc->abort = 1;
+                    set_error(p.err, PK_DEVERR_TIMEOUT);
+                }
+                break;
+            }
+            const uint32_t vfull = smem_u32(&misc->vfull[vst]);
+            if (lane == 0) mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
+            __syncwarp();
+            // V: one box per page, [half][row][64] at the page's slot.
+            if (ok) tma_load_5d(base + kVOff + vst * kVBytes + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, h, phys);
+            ++vissued;
+            if (i + 1 < nT) phys_next = fetch(i + 1);
         }
         if (misc->abort && lane == 0) {
+            // Let the copies in flight land before the CTA can exit.
             mbar_wait(smem_u32(&misc->q_full), 0, &misc->never, kWaitLimitNs);
-            for (int i = max(0, issued - kStages); i < issued; ++i) {
-                mbar_wait(smem_u32(&misc->full[i % kStages]), (i / kStages) & 1, &misc->never, kWaitLimitNs);
-                mbar_wait(smem_u32(&misc->vfull[i % kStages]), (i / kStages) & 1, &misc->never, kWaitLimitNs);
-            }
+            for (int i = max(0, kissued - kKStages); i < kissued; ++i)
+                mbar_wait(smem_u32(&misc->kfull[i % kKStages]), (i / kKStages) & 1, &misc->never, kWaitLimitNs);
+            for (int i = max(0, vissued - kVStages); i < vissued; ++i)
+                mbar_wait(smem_u32(&misc->vfull[i % kVStages]), (i / kVStages) & 1, &misc->never, kWaitLimitNs);
         }
     }
     else if (warp == 1) {
         // ================= MMA issuer =================
-        // S of tile i is issued before P.V of tile i-1, so the scores of the
-        // next tile are computed while the softmax works on the current one.
+        // Key tile i: for query tile 0, P.V of tile i-1 (its P lies in the
+        // columns S(i) overwrites, so it goes first) and then S(i); the same
+        // for query tile 1.  Meanwhile the softmax of the other query tile
+        // runs.
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kRows, kKeys, 0, 0);   // A = Q, B = K, both K-major
             constexpr uint32_t kIdescO = idesc_bf16(kRows, D, 0, 1);       // A = P (TMEM), B = V (MN-major)
             bool alive = mbar_wait(smem_u32(&misc->q_full), 0, &misc->abort, kWaitLimitNs);
-            auto pv = [&](int t) {
-                alive = alive && mbar_wait(smem_u32(&misc->p_full), t & 1, &misc->abort, kWaitLimitNs) &&
-                        mbar_wait(smem_u32(&misc->vfull[t % kStages]), (t / kStages) & 1, &misc->abort,
-                                  kWaitLimitNs);
-                if (!alive) return;
-                tc_fence_after();
-                const uint32_t vbase = stage_addr + (t % kStages) * kStageBytes + kVOff;
+            for (int i = 0; i <= nT && alive; ++i) {
+                for (int x = 0; x < 2; ++x) {
+                    const int nx = x ? n1 : n0;
+                    const uint32_t s_col = tmem + kTmemS + x * 128;
+                    if (i >= 1 && i - 1 < nx) {
+                        const int t = i - 1;
+                        alive = mbar_wait(smem_u32(&misc->p_full[x]), t & 1, &misc->abort, kWaitLimitNs) &&
+                                mbar_wait(smem_u32(&misc->vfull[t % kVStages]), (t / kVStages) & 1, &misc->abort,
+                                          kWaitLimitNs);
+                        if (!alive) break;
+                        tc_fence_after();
+                        const uint32_t vbase = base + kVOff + (t % kVStages) * kVBytes;
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    // Keys 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
-                    const uint32_t t0 = kk * 16;
-                    const uint64_t b = smem_desc(vbase + (t0 / B) * v_page + (t0 % B) * 128, v_half, v_group,
-                                                 kLayoutSw128);
-                    mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + (t & 1) * 64 + kk * 8, b, kIdescO,
-                                    (t > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kKeys / 16; ++kk) {
+                            // Keys 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
+                            const uint32_t k0 = kk * 16;
+                            const uint64_t b = smem_desc(vbase + (k0 / B) * v_page + (k0 % B) * 128, v_half,
+                                                         v_group, kLayoutSw128);
+                            mma_bf16_tmem_a(tmem + kTmemO + x * 128, s_col + kk * 8, b, kIdescO,
+                                            (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(smem_u32(&misc->pv_done[x]));
+                    }
+                    if (i < nx) {
+                        alive = mbar_wait(smem_u32(&misc->kfull[i % kKStages]), (i / kKStages) & 1, &misc->abort,
+                                          kWaitLimitNs);
+                        if (!alive) break;
+                        tc_fence_after();
+                        const uint32_t kbase = base + kKOff + (i % kKStages) * kKBytes;
+                        const uint32_t qbase = base + kQOff + x * kQBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+                            const uint64_t a = smem_desc(qbase + off, 16, 1024, kLayoutSw128);
+                            const uint64_t b = smem_desc(kbase + off, 16, 1024, kLayoutSw128);
+                            mma_bf16(s_col, a, b, kIdescS, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(smem_u32(&misc->s_full[x]));
+                    }
                 }
-                mma_commit(smem_u32(&misc->pv_done[t & 1]));
-                mma_commit(smem_u32(&misc->empty[t % kStages]));
-            };
-            for (int i = 0; i < n_tiles && alive; ++i) {
-                const int st = i % kStages;
-                alive = mbar_wait(smem_u32(&misc->full[st]), (i / kStages) & 1, &misc->abort, kWaitLimitNs);
                 if (!alive) break;
-                tc_fence_after();
-                const uint32_t kbase = stage_addr + st * kStageBytes + kKOff;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-                    const uint64_t a = smem_desc(q_addr + off, 16, 1024, kLayoutSw128);
-                    const uint64_t b = smem_desc(kbase + off, 16, 1024, kLayoutSw128);
-                    mma_bf16(tmem + kTmemS + (i & 1) * kKeys, a, b, kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&misc->s_full[i & 1]));
-                if (i > 0) pv(i - 1);
+                if (i >= 1) mma_commit(smem_u32(&misc->vempty[(i - 1) % kVStages]));   // both P.V of tile i-1
+                if (i < nT) mma_commit(smem_u32(&misc->kempty[i % kKStages]));         // both S of tile i
             }
-            if (alive) pv(n_tiles - 1);
             if (!alive) {
                 misc->abort = 1;
                 set_error(p.err, PK_DEVERR_TIMEOUT);
@@ -293,42 +349,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         __syncwarp();
     }
     else {
-        // ================= softmax (warps 2-5): thread <-> query row =================
-        const int quad = warp & 3;
+        // ================= softmax: warps 2-5 tile 0, 6-9 tile 1; thread <-> query row =================
+        const int x = (warp - 2) >> 2;
+        const int nx = x ? n1 : n0;
+        const int quad = warp & 3;                      // TMEM lanes 32 * (warp % 4) ..
         const int row = quad * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const uint32_t s_col = lane_addr + kTmemS + x * 128;
+        const uint32_t o_col = lane_addr + kTmemO + x * 128;
+        const int tok0 = qt0 + x * QT;                  // first query token of this tile
         const int rr = row / G;                         // query token of this row (rows are token * G + head)
-        const int qp = pos0 + qt0 + rr;                 // its position: it sees keys 0 .. qp
+        const int qp = pos0 + tok0 + rr;                // its position: it sees keys 0 .. qp
         float m_ref = -INFINITY, l_run = 0.f;
-        bool alive = true;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int st = i % kStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->s_full[i & 1]), (i >> 1) & 1, &misc->never,
-                                                   kWaitLimitNs))) {
+        bool alive = nx > 0;
+        for (int i = 0; i < nx; ++i) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->s_full[x]), i & 1, &misc->abort, kWaitLimitNs))) {
                 alive = false;
                 break;
             }
             tc_fence_after();
+            // The row's 128 scores of this tile into registers for the max
+            // (two loads in flight, one wait).
+            uint32_t sa[64], sb[64];
+            tmemw::ld64(s_col, sa);
+            tmemw::ld64(s_col + 64, sb);
             uint32_t msk[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) msk[c] = misc->mask[st][c];
-            const int kbase = i * kKeys;
-            const uint32_t sbase = lane_addr + kTmemS + (i & 1) * kKeys;
-            // The row's 128 scores of this tile into registers (two loads in
-            // flight, one wait).
-            uint32_t sa[64], sb[64];
-            tmemw::ld64(sbase, sa);
-            tmemw::ld64(sbase + 64, sb);
-            // This tile's P buffer is free once P.V of tile i - 2 is done (long ago).
-            if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[i & 1]), ((i - 2) >> 1) & 1,
-                                                             &misc->never, kWaitLimitNs))) {
-                alive = false;
-                break;
-            }
+            for (int c = 0; c < 4; ++c) msk[c] = misc->mask[i % kMaskRing][c];
             tmemw::wait_ld(sa);
             tmemw::wait_ld(sb);
-            tc_fence_after();
-            const uint32_t pbase = lane_addr + kTmemP + (i & 1) * 64;
+            const int kbase = i * kKeys;
             auto score = [&](int k) -> float { return __uint_as_float(k < 64 ? sa[k] : sb[k - 64]); };
             // Key k of the tile is visible to this row if its page was
             // loaded and it is not after the row's own position.
@@ -348,7 +398,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             auto gather = [&](auto easy_tag) {
                 constexpr bool kEasy = decltype(easy_tag)::value;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ext[e] = kEasy ? score(e) : (visible(e) ? score(e) : __int_as_float(0x7fffffff));
+                for (int e = 0; e < 8; ++e)
+                    ext[e] = kEasy ? score(e) : (visible(e) ? score(e) : __int_as_float(0x7fffffff));
 #pragma unroll
                 for (int k = 8; k < kKeys; ++k) {
                     const float v = kEasy ? score(k) : (visible(k) ? score(k) : __int_as_float(0x7fffffff));
@@ -371,9 +422,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 // denominator (rare after the first tile).
                 const float mn = need ? tmax : m_ref;
                 const float a = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - mn);
-                // O holds tiles up to i - 1: wait for that P.V (the only wait on it).
-                if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[(i - 1) & 1]),
-                                                                ((i - 1) >> 1) & 1, &misc->never, kWaitLimitNs))) {
+                // O holds key tiles up to i - 1: wait for that P.V.
+                if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[x]), (i - 1) & 1,
+                                                                &misc->abort, kWaitLimitNs))) {
                     alive = false;
                     break;
                 }
@@ -382,30 +433,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int cc = 0; cc < D / 8; ++cc) {
                         float ov[8];
-                        tmem_ld<8>(lane_addr + kTmemO + cc * 8, ov);
+                        tmem_ld<8>(o_col + cc * 8, ov);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) ov[k] *= a;
-                        tmem_st8(lane_addr + kTmemO + cc * 8, ov);
+                        tmem_st8(o_col + cc * 8, ov);
                     }
                 }
                 l_run *= a;
                 m_ref = mn;
             }
-            // p = 2^(c * s - m_ref) as bf16 pairs into this tile's P columns of
-            // TMEM (the P.V MMA's A operand); the denominator sums the bf16
-            // weights the MMA actually applies, in four chains.
+            // p = 2^(c * s - m_ref) as bf16 pairs over the first 64 columns
+            // of S (the P.V MMA's A operand); the denominator sums the bf16
+            // weights the MMA actually applies, in four chains.  The scores
+            // are read again, 32 columns at a time with the next load in
+            // flight (fewer live registers than keeping all 128): P of
+            // columns 32cc.. goes to columns 16cc.., already read.
             const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
             auto emit = [&](auto easy_tag) {
                 constexpr bool kEasy = decltype(easy_tag)::value;
+                uint32_t cb[2][32];
+                tmemw::ld32(s_col, cb[0]);
+                tmemw::wait_ld(cb[0]);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
+                    if (cc < 3) tmemw::ld32(s_col + 32 * (cc + 1), cb[(cc + 1) & 1]);
                     uint32_t packed[16];
 #pragma unroll
                     for (int k = 0; k < 32; k += 2) {
                         const int kk = cc * 32 + k;
-                        float p0 = fast_exp2(fmaf(score(kk), c, nm));
-                        float p1 = fast_exp2(fmaf(score(kk + 1), c, nm));
+                        float p0 = fast_exp2(fmaf(__uint_as_float(cb[cc & 1][k]), c, nm));
+                        float p1 = fast_exp2(fmaf(__uint_as_float(cb[cc & 1][k + 1]), c, nm));
                         if constexpr (!kEasy) {
                             p0 = visible(kk) ? p0 : 0.f;
                             p1 = visible(kk + 1) ? p1 : 0.f;
@@ -414,7 +472,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         packed[k / 2] = w;
                         ls[(k / 2) & 3] += bf16_lo(w) + bf16_hi(w);
                     }
-                    tmem_st16(pbase + cc * 16, packed);   // keys 32cc .. 32cc+31 of this row
+                    tmem_st16(s_col + cc * 16, packed);   // keys 32cc .. 32cc+31 of this row
+                    if (cc < 3) tmemw::wait_ld(cb[(cc + 1) & 1]);
                 }
             };
             if (easy) emit(std::true_type{});
@@ -422,21 +481,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // V rows of keys outside the sequence or behind a bad table entry
             // may hold stale or non-finite bits; the MMA multiplies them by 0,
-            // so zero them (thread <-> key row) once V has landed.
+            // so zero them (thread <-> key row) once V has landed.  The group
+            // of the first query tile that uses this key tile does it, before
+            // its P.V is issued (the other tile's P.V follows).
             const int wrow = row >> 5;                      // select, not an indexed load: msk stays in registers
             const uint32_t mrow = wrow == 0 ? msk[0] : wrow == 1 ? msk[1] : wrow == 2 ? msk[2] : msk[3];
-            const bool bad = !((mrow >> (row & 31)) & 1u);
+            const bool bad = !((mrow >> (row & 31)) & 1u) && (x == 0 || i >= n0);
             if (__any_sync(0xffffffffu, bad)) {
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->vfull[st]), (i / kStages) & 1, &misc->never,
-                                                       kWaitLimitNs))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->vfull[i % kVStages]), (i / kVStages) & 1,
+                                                       &misc->abort, kWaitLimitNs))) {
                     alive = false;
                     break;
                 }
                 if (bad) {
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch) {
-                        uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + (row / B) * v_page +
-                                                                ch * B * 128 + (row % B) * 128);
+                        uint4 *vrow = reinterpret_cast<uint4 *>(smem + kVOff + (i % kVStages) * kVBytes +
+                                                                (row / B) * v_page + ch * B * 128 + (row % B) * 128);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
                     }
@@ -446,29 +507,80 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             fence_proxy_async_smem();       // zeroed V rows are visible to the MMA
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&misc->p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&misc->p_full[x]));
         }
-        if (alive && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[(n_tiles - 1) & 1]),
-                                                         ((n_tiles - 1) >> 1) & 1,
-                                                         &misc->never, kWaitLimitNs)))
+        if (alive && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[x]), (nx - 1) & 1, &misc->abort,
+                                                         kWaitLimitNs)))
             alive = false;
-        if (!alive) {
+        if (!alive && nx > 0) {
             misc->abort = 1;
             set_error(p.err, PK_DEVERR_TIMEOUT);
-        } else {
+        }
+        // One decision for the whole group (every warp reaches this barrier;
+        // the TMA-store path below has another).
+        if (!named_bar_or(1 + x, 128, !alive)) {
             tc_fence_after();
-            // O / l of this row to out[q0 + qt0 + token, h * G + head, :].
-            const bool store = qt0 + rr < qn;
+            // O / l of this row to out[q0 + tok0 + token, h * G + head, :].
+            const int ntok = min(qn - tok0, QT);
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            const size_t obase =
-                (static_cast<size_t>(q0 + qt0 + rr) * H + h * G + (row & (G - 1))) * static_cast<size_t>(D);
+            if (o_tma && ntok == QT) {
+                // A full tile: bf16 rows into this tile's Q buffer (free: its
+                // last S is done) in the 128-byte-swizzled layout of the
+                // output map's box, then one TMA store per 64 columns.
+                uint8_t *obuf = smem + kQOff + x * kQBytes;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float ov[32];
-                tmem_ld<32>(lane_addr + kTmemO + c * 32, ov);
-                if (store) {
+                for (int ch = 0; ch < NCH; ++ch) {
+                    uint32_t ov[64];
+                    tmemw::ld64(o_col + ch * 64, ov);
+                    tmemw::wait_ld(ov);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) store_row_out(p, obase + c * 32 + k, ov[k] * inv);
+                    for (int jj = 0; jj < 8; ++jj) {
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(ov[8 * jj + 0]) * inv, __uint_as_float(ov[8 * jj + 1]) * inv);
+                        u.y = pack_bf16x2(__uint_as_float(ov[8 * jj + 2]) * inv, __uint_as_float(ov[8 * jj + 3]) * inv);
+                        u.z = pack_bf16x2(__uint_as_float(ov[8 * jj + 4]) * inv, __uint_as_float(ov[8 * jj + 5]) * inv);
+                        u.w = pack_bf16x2(__uint_as_float(ov[8 * jj + 6]) * inv, __uint_as_float(ov[8 * jj + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(obuf + ch * kChunk + row * 128 + ((jj ^ (row & 7)) << 4)) = u;
+                    }
+                }
+                fence_proxy_async_smem();
+                group_bar(1 + x);
+                if (quad == 2 && lane == 0) {               // one thread of the group
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+                        tma_store_3d(&tm_o, base + kQOff + x * kQBytes + ch * kChunk, ch * 64, h * G, q0 + tok0);
+                    bulk_commit();
+                    bulk_wait_read();                       // the buffer stays until the copy has read it
+                }
+            } else {
+                const bool store = rr < ntok;
+                const size_t obase =
+                    (static_cast<size_t>(q0 + tok0 + rr) * H + h * G + (row & (G - 1))) * static_cast<size_t>(D);
+                const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0;
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    uint32_t ov[64];
+                    tmemw::ld64(o_col + ch * 64, ov);
+                    tmemw::wait_ld(ov);
+                    if (!store) continue;
+                    float f[64];
+#pragma unroll
+                    for (int k = 0; k < 64; ++k) f[k] = __uint_as_float(ov[k]) * inv;
+                    if (vec && p.out_fp32) {
+                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + obase + ch * 64);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+                    } else if (vec) {
+                        uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + obase + ch * 64);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            o[k] = make_uint4(pack_bf16x2(f[8 * k], f[8 * k + 1]), pack_bf16x2(f[8 * k + 2], f[8 * k + 3]),
+                                              pack_bf16x2(f[8 * k + 4], f[8 * k + 5]),
+                                              pack_bf16x2(f[8 * k + 6], f[8 * k + 7]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k) store_row_out(p, obase + ch * 64 + k, f[k]);
+                    }
                 }
             }
         }
@@ -499,7 +611,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-// A tiled map with the 128-byte swizzle the MMA descriptors expect.
+// A tiled bf16 map with the 128-byte swizzle the MMA descriptors expect.
 bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
             const cuuint32_t *box) {
     auto enc = encoder();
@@ -521,13 +633,20 @@ cudaError_t launch_dg(const DecodeParams &p, int max_q_len, cudaStream_t stream)
     const cuuint64_t vdims[5] = {64, B, Dd / 64, Hkv, P};
     const cuuint64_t vstr[4] = {Hkv * Dd * 2, 128, Dd * 2, B * Hkv * Dd * 2};
     const cuuint32_t vbox[5] = {64, static_cast<cuuint32_t>(B), static_cast<cuuint32_t>(Dd / 64), 1, 1};
+    // Queries (and bf16 outputs) [total_q, H, D]: box (64 elements, G heads,
+    // 128 / G tokens) = one query tile, row = token * G + head.
     const cuuint64_t qdims[3] = {Dd, static_cast<cuuint64_t>(p.num_heads), static_cast<cuuint64_t>(p.total_q)};
     const cuuint64_t qstr[2] = {Dd * 2, Dd * p.num_heads * 2};
     const cuuint32_t qbox[3] = {64, G, kRows / G};
-    CUtensorMap mk, mv, mq;
+    CUtensorMap mk, mv, mq, mo;
     if (!encode(&mk, p.k_cache, 4, cdims, cstr, cbox) || !encode(&mv, p.v_cache, 5, vdims, vstr, vbox) ||
         !encode(&mq, p.q, 3, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
+    // Full tiles of a bf16 output go out by TMA store; otherwise (fp32, or
+    // an output the map does not accept) by plain stores.
+    int o_tma = 0;
+    if (!p.out_fp32 && encode(&mo, p.out, 3, qdims, qstr, qbox)) o_tma = 1;
+    else mo = mq;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -535,11 +654,12 @@ cudaError_t launch_dg(const DecodeParams &p, int max_q_len, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int qblocks = (max_q_len + kRows / G - 1) / (kRows / G);
+    const int qblocks = (max_q_len + 2 * (kRows / G) - 1) / (2 * (kRows / G));
     const int64_t grid = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * qblocks;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    prefill_tc_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mk, mv, mq, p, qblocks);
+    prefill_tc_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mk, mv, mq, mo, p, qblocks,
+                                                                                           o_tma);
     return cudaGetLastError();
 }
 
