@@ -181,6 +181,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const uint32_t v_page = static_cast<uint32_t>(B) * 128u * NCH;
     const uint32_t v_half = static_cast<uint32_t>(B) * 128u;        // between the two 64-element halves
     const uint32_t v_group = B >= 16 ? 1024u : v_page;              // between groups of 8 tokens
+    const int lgB = __ffs(B) - 1;                                    // B is a power of two
     constexpr bool mq = MQ;                           // several query tokens per sequence
     Slot *slots = static_cast<Slot *>(p.tc_slots);
 
@@ -390,7 +391,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     // Tokens 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
                     const uint32_t t0 = kk * 16;
-                    const uint64_t a = smem_desc(vbase + (t0 / B) * v_page + (t0 % B) * 128, v_half, v_group,
+                    const uint64_t a = smem_desc(vbase + (t0 >> lgB) * v_page + (t0 & (B - 1)) * 128, v_half, v_group,
                                                  kLayoutSw128);
                     const uint64_t b = smem_desc(pbase + kk * 512, 256, 128, kLayoutNone);
                     mma_bf16(tmem + kTmemO + (sg & 1) * kNPad, a, b, kIdescPV, (first && kk == 0) ? 0u : 1u);
@@ -649,8 +650,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 // masked tokens may hold stale or non-finite bits, so zero them.
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
-                    uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + (row / B) * v_page +
-                                                            ch * B * 128 + (row % B) * 128);
+                    uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + (row >> lgB) * v_page +
+                                                            ch * B * 128 + (row & (B - 1)) * 128);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
                 }

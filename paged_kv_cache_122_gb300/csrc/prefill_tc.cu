@@ -130,6 +130,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint32_t v_page = static_cast<uint32_t>(B) * 128u * NCH;
     const uint32_t v_half = static_cast<uint32_t>(B) * 128u;        // between the two 64-element halves
     const uint32_t v_group = B >= 16 ? 1024u : v_page;              // between groups of 8 keys
+    const int lgB = __ffs(B) - 1;                                    // B is a power of two
     int L = p.seq_lens[s];
     const int q0 = p.cu_q_lens[s];
     const int qn = p.cu_q_lens[s + 1] - q0;
@@ -310,7 +311,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         for (int kk = 0; kk < kKeys / 16; ++kk) {
                             // Keys 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
                             const uint32_t k0 = kk * 16;
-                            const uint64_t b = smem_desc(vbase + (k0 / B) * v_page + (k0 % B) * 128, v_half,
+                            const uint64_t b = smem_desc(vbase + (k0 >> lgB) * v_page + (k0 & (B - 1)) * 128, v_half,
                                                          v_group, kLayoutSw128);
                             mma_bf16_tmem_a(tmem + kTmemO + x * 128, s_col + kk * 8, b, kIdescO,
                                             (t > 0 || kk > 0) ? 1u : 0u);
@@ -497,7 +498,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch) {
                         uint4 *vrow = reinterpret_cast<uint4 *>(smem + kVOff + (i % kVStages) * kVBytes +
-                                                                (row / B) * v_page + ch * B * 128 + (row % B) * 128);
+                                                                (row >> lgB) * v_page + ch * B * 128 + (row & (B - 1)) * 128);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
                     }
