@@ -25,10 +25,11 @@
 // its A operand; the next S of that tile is issued after that P.V, and
 // tcgen05 MMAs of one thread execute in issue order.
 //
-// Per CTA (320 threads):
+// Per CTA (352 threads):
 //   warp 0     producer: both Q tiles once, then per key tile the K rows
-//              of each page (two 64-element halves) into a K ring and the
-//              V rows of each page (one box) into a V ring;
+//              of each page (two 64-element halves) into a K ring;
+//   warp 10    producer: per key tile the V rows of each page (one box)
+//              into a V ring;
 //   warp 1     MMA issuer (one thread): per key tile i, P.V(i-1) then S(i)
 //              for tile 0, then the same for tile 1;
 //   warps 2-5  softmax of tile 0, warps 6-9 softmax of tile 1: row max
@@ -57,7 +58,7 @@ constexpr int kKeys = 128;                      // keys per tile = MMA N of S
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kMaskRing = 4;                    // tile masks in flight (producer runs <= 2 tiles ahead)
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr uint32_t kChunk = 128 * 128;          // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kQBytes = 2 * kChunk;        // one query tile (D <= 128)
 constexpr uint32_t kKBytes = 2 * kChunk;        // K of one key tile
@@ -182,12 +183,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = misc->tmem_base;
 
-    if (warp == 0) {
-        // ================= producer =================
+    if (warp == 0 || warp == 10) {
+        // ================= producers: warp 0 the queries and K, warp 10 V =================
+        // (Two warps, so that the copies of K and of V are issued side by side.)
+        const bool kprod = warp == 0;
         const int MB = p.max_blocks_per_seq;
-        if (lane == 0) {
+        if (kprod && lane == 0) {
             prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
             const uint32_t qf = smem_u32(&misc->q_full);
             const int tiles = n1 > 0 ? 2 : 1;
             mbar_arrive_expect_tx(qf, tiles * kRows * 128u * NCH);
@@ -198,6 +200,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                                 q0 + qt0 + x * QT);
             }
         }
+        if (!kprod && lane == 0) prefetch_tmap(&tm_v);
         // Block-table entries of a key tile, one page per lane; the next
         // tile's are fetched while the current tile's copies are issued.
         auto fetch = [&](int t) -> int {
@@ -205,14 +208,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const int pg = (min(kKeys, L - tok) + B - 1) / B;
             return lane < pg ? p.block_tables[static_cast<size_t>(s) * MB + tok / B + lane] : -1;
         };
+        const int nstages = kprod ? kKStages : kVStages;
         int phys_next = fetch(0);
-        int kissued = 0, vissued = 0;
+        int issued = 0;
         for (int i = 0; i < nT; ++i) {
-            const int kst = i % kKStages, vst = i % kVStages;
+            const int st = i % nstages;
             const int phys_raw = phys_next;
             int got = 1;
             if (lane == 0)
-                got = mbar_wait(smem_u32(&misc->kempty[kst]), ((i / kKStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
+                got = mbar_wait(smem_u32(kprod ? &misc->kempty[st] : &misc->vempty[st]), ((i / nstages) & 1) ^ 1,
+                                &misc->abort, kWaitLimitNs);
             if (!__shfl_sync(0xffffffffu, got, 0)) {
                 if (lane == 0) {
                     misc->abort = 1;
@@ -228,61 +233,53 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             if (lane < pages) {
                 phys = phys_raw;
                 ok = phys >= 0 && phys < p.num_blocks;
-                if (!ok) set_error(p.err, PK_DEVERR_BLOCK_ID);
+                if (!ok && kprod) set_error(p.err, PK_DEVERR_BLOCK_ID);
             }
-            uint32_t bits = 0;
-            const int r0 = lane * B;
-            if (ok) {
-                const int nrows = min(B, vlen - r0);
-                bits = (nrows >= 32 ? 0xffffffffu : ((1u << nrows) - 1u)) << (r0 & 31);
-            }
-            const int word = r0 >> 5;
-            const uint32_t m0 = __reduce_or_sync(0xffffffffu, word == 0 ? bits : 0u);
-            const uint32_t m1 = __reduce_or_sync(0xffffffffu, word == 1 ? bits : 0u);
-            const uint32_t m2 = __reduce_or_sync(0xffffffffu, word == 2 ? bits : 0u);
-            const uint32_t m3 = __reduce_or_sync(0xffffffffu, word == 3 ? bits : 0u);
             const uint32_t nok = __popc(__ballot_sync(0xffffffffu, ok));
-            const uint32_t kfull = smem_u32(&misc->kfull[kst]);
-            if (lane == 0) {
-                uint32_t *mk = misc->mask[i % kMaskRing];
-                mk[0] = m0;
-                mk[1] = m1;
-                mk[2] = m2;
-                mk[3] = m3;
-                mbar_arrive_expect_tx(kfull, nok * B * 128u * NCH);
-            }
-            __syncwarp();
-            if (ok) {
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_4d(base + kKOff + kst * kKBytes + ch * kChunk + r0 * 128, &tm_k, kfull, ch * 64, h, 0,
-                                phys);
-            }
-            ++kissued;
-            if (lane == 0)
-                got = mbar_wait(smem_u32(&misc->vempty[vst]), ((i / kVStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
-            if (!__shfl_sync(0xffffffffu, got, 0)) {
-                if (lane == 0) {
-                    misc->abort = 1;
-                    set_error(p.err, PK_DEVERR_TIMEOUT);
+            const int r0 = lane * B;
+            if (kprod) {
+                uint32_t bits = 0;
+                if (ok) {
+                    const int nrows = min(B, vlen - r0);
+                    bits = (nrows >= 32 ? 0xffffffffu : ((1u << nrows) - 1u)) << (r0 & 31);
                 }
-                break;
+                const int word = r0 >> 5;
+                const uint32_t m0 = __reduce_or_sync(0xffffffffu, word == 0 ? bits : 0u);
+                const uint32_t m1 = __reduce_or_sync(0xffffffffu, word == 1 ? bits : 0u);
+                const uint32_t m2 = __reduce_or_sync(0xffffffffu, word == 2 ? bits : 0u);
+                const uint32_t m3 = __reduce_or_sync(0xffffffffu, word == 3 ? bits : 0u);
+                const uint32_t kfull = smem_u32(&misc->kfull[st]);
+                if (lane == 0) {
+                    uint32_t *mk = misc->mask[i % kMaskRing];
+                    mk[0] = m0;
+                    mk[1] = m1;
+                    mk[2] = m2;
+                    mk[3] = m3;
+                    mbar_arrive_expect_tx(kfull, nok * B * 128u * NCH);
+                }
+                __syncwarp();
+                if (ok) {
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+                        tma_load_4d(base + kKOff + st * kKBytes + ch * kChunk + r0 * 128, &tm_k, kfull, ch * 64, h, 0,
+                                    phys);
+                }
+            } else {
+                const uint32_t vfull = smem_u32(&misc->vfull[st]);
+                if (lane == 0) mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
+                __syncwarp();
+                // V: one box per page, [half][row][64] at the page's slot.
+                if (ok) tma_load_5d(base + kVOff + st * kVBytes + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, h, phys);
             }
-            const uint32_t vfull = smem_u32(&misc->vfull[vst]);
-            if (lane == 0) mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
-            __syncwarp();
-            // V: one box per page, [half][row][64] at the page's slot.
-            if (ok) tma_load_5d(base + kVOff + vst * kVBytes + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, h, phys);
-            ++vissued;
+            ++issued;
             if (i + 1 < nT) phys_next = fetch(i + 1);
         }
         if (misc->abort && lane == 0) {
             // Let the copies in flight land before the CTA can exit.
-            mbar_wait(smem_u32(&misc->q_full), 0, &misc->never, kWaitLimitNs);
-            for (int i = max(0, kissued - kKStages); i < kissued; ++i)
-                mbar_wait(smem_u32(&misc->kfull[i % kKStages]), (i / kKStages) & 1, &misc->never, kWaitLimitNs);
-            for (int i = max(0, vissued - kVStages); i < vissued; ++i)
-                mbar_wait(smem_u32(&misc->vfull[i % kVStages]), (i / kVStages) & 1, &misc->never, kWaitLimitNs);
+            if (kprod) mbar_wait(smem_u32(&misc->q_full), 0, &misc->never, kWaitLimitNs);
+            for (int i = max(0, issued - nstages); i < issued; ++i)
+                mbar_wait(smem_u32(kprod ? &misc->kfull[i % nstages] : &misc->vfull[i % nstages]), (i / nstages) & 1,
+                          &misc->never, kWaitLimitNs);
         }
     }
     else if (warp == 1) {
@@ -349,7 +346,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         __syncwarp();
     }
-    else {
+    else if (warp < 10) {
         // ================= softmax: warps 2-5 tile 0, 6-9 tile 1; thread <-> query row =================
         const int x = (warp - 2) >> 2;
         const int nx = x ? n1 : n0;
