@@ -55,9 +55,9 @@ using namespace sm100;
 
 constexpr int kRows = 128;                      // query rows per tile = MMA M
 constexpr int kKeys = 128;                      // keys per tile = MMA N of S
-constexpr int kKStages = 2;
+constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kMaskRing = 4;                    // tile masks in flight (producer runs <= 2 tiles ahead)
+constexpr int kMaskRing = 4;                    // tile masks in flight (the K producer runs <= 3 tiles ahead)
 constexpr int kThreads = 352;
 constexpr uint32_t kChunk = 128 * 128;          // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kQBytes = 2 * kChunk;        // one query tile (D <= 128)
@@ -105,6 +105,71 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void group_bar(uint32_t id) {
     asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// Three-input max / min (NaN inputs are skipped, as by fmaxf / fminf).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// 2^x of a pair on the FMA pipe (the softmax gives a share of its
+// exponentials to it, the rest to the SFU).  x = n + f with n = floor(x) --
+// adding 1.5 * 2^23 rounded toward -inf leaves n in the low mantissa bits --
+// and f in [0, 1); 2^f is a cubic, 2^n is added to the exponent field.  The
+// cubic's coefficients are the minimax fit of 2^f on [0, 1) for relative
+// error (solved as a linear programme over 4,096 points): relative error
+// below 7.5e-5 (1.1e-4 with fp32 evaluation), far under the bf16 rounding
+// the weights get next.  x is clamped to -126 first, so that the exponent
+// field cannot wrap (a weight below 2^-126 is 0 to bf16 precision in a sum
+// of weights near 1).
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x) {
+    constexpr float kMagic = 12582912.0f;                   // 1.5 * 2^23
+    constexpr float kC0 = 0.99992520f, kC1 = 0.69583356f, kC2 = 0.22606714f, kC3 = 0.07802454f;
+    float xl, xh;
+    f2_split(x, xl, xh);
+    asm("max.NaN.f32 %0, %0, 0fC2FC0000;" : "+f"(xl));     // max(x, -126), NaN stays NaN
+    asm("max.NaN.f32 %0, %0, 0fC2FC0000;" : "+f"(xh));
+    x = f2(xl, xh);
+    const uint64_t m2 = f2(kMagic, kMagic);
+    uint64_t t, n, fr;
+    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(t) : "l"(x), "l"(m2));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(n) : "l"(t), "l"(m2));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(fr) : "l"(x), "l"(n));
+    uint64_t pp = ffma2(f2(kC3, kC3), fr, f2(kC2, kC2));
+    pp = ffma2(pp, fr, f2(kC1, kC1));
+    pp = ffma2(pp, fr, f2(kC0, kC0));
+    float pl, ph, tl, th;
+    f2_split(pp, pl, ph);
+    f2_split(t, tl, th);
+    // t's bits are those of 1.5 * 2^23 plus n; shifted by 23 only n << 23 remains.
+    return f2(__uint_as_float(__float_as_uint(pl) + (__float_as_uint(tl) << 23)),
+              __uint_as_float(__float_as_uint(ph) + (__float_as_uint(th) << 23)));
 }
 
 // grid: one CTA per (sequence, KV head, pair of query tiles of 128 / G
@@ -365,6 +430,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 alive = false;
                 break;
             }
+            // Tile 1's group starts half a period behind tile 0's (it
+            // begins key tile 0 once tile 0 has finished it), so that the
+            // MMAs of one group run while the other computes.
+            if (x == 1 && i == 0 && n0 > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->p_full[0]), 0, &misc->abort, kWaitLimitNs))) {
+                alive = false;
+                break;
+            }
             tc_fence_after();
             // The row's 128 scores of this tile into registers for the max
             // (two loads in flight, one wait).
@@ -393,25 +466,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             // products).  Eight independent chains; a masked key is NaN,
             // which fmaxf / fminf skip.
             float ext[8];
-            auto gather = [&](auto easy_tag) {
+            auto gather = [&](auto easy_tag, auto max_tag) {
                 constexpr bool kEasy = decltype(easy_tag)::value;
+                constexpr bool kMax = decltype(max_tag)::value;
+                auto v = [&](int k) -> float {
+                    return kEasy ? score(k) : (visible(k) ? score(k) : __int_as_float(0x7fffffff));
+                };
+                auto pick3 = [&](float a, float b, float d) { return kMax ? max3(a, b, d) : min3(a, b, d); };
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    ext[e] = kEasy ? score(e) : (visible(e) ? score(e) : __int_as_float(0x7fffffff));
+                for (int e = 0; e < 8; ++e) ext[e] = v(e);
 #pragma unroll
-                for (int k = 8; k < kKeys; ++k) {
-                    const float v = kEasy ? score(k) : (visible(k) ? score(k) : __int_as_float(0x7fffffff));
-                    ext[k & 7] = c >= 0.f ? fmaxf(ext[k & 7], v) : fminf(ext[k & 7], v);
+                for (int k = 8; k + 16 <= kKeys; k += 16) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ext[e] = pick3(ext[e], v(k + e), v(k + 8 + e));
                 }
-            };
-            if (easy) gather(std::true_type{});
-            else gather(std::false_type{});
-            float e4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) e4[e] = c >= 0.f ? fmaxf(ext[e], ext[e + 4]) : fminf(ext[e], ext[e + 4]);
-            const float e2a = c >= 0.f ? fmaxf(e4[0], e4[2]) : fminf(e4[0], e4[2]);
-            const float e2b = c >= 0.f ? fmaxf(e4[1], e4[3]) : fminf(e4[1], e4[3]);
-            const float ex = c >= 0.f ? fmaxf(e2a, e2b) : fminf(e2a, e2b);
+                for (int e = 0; e < 8; ++e) ext[e] = kMax ? fmaxf(ext[e], v(kKeys - 8 + e)) : fminf(ext[e], v(kKeys - 8 + e));
+                const float e0 = pick3(ext[0], ext[1], ext[2]), e1 = pick3(ext[3], ext[4], ext[5]);
+                return pick3(e0, e1, kMax ? fmaxf(ext[6], ext[7]) : fminf(ext[6], ext[7]));
+            };
+            const float ex = easy ? (c >= 0.f ? gather(std::true_type{}, std::true_type{})
+                                             : gather(std::true_type{}, std::false_type{}))
+                                  : (c >= 0.f ? gather(std::false_type{}, std::true_type{})
+                                             : gather(std::false_type{}, std::false_type{}));
             // No visible key (NaN): no candidate for the reference max.
             const float tmax = ex == ex ? ex * c : -INFINITY;
             const bool need = tmax > m_ref + kRescaleLog2;
@@ -447,7 +524,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             // flight (fewer live registers than keeping all 128): P of
             // columns 32cc.. goes to columns 16cc.., already read.
             const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t c2 = f2(c, c), nm2 = f2(nm, nm);
+            uint64_t lacc[2] = {0ull, 0ull};           // (+0, +0) pairs
             auto emit = [&](auto easy_tag) {
                 constexpr bool kEasy = decltype(easy_tag)::value;
                 uint32_t cb[2][32];
@@ -460,15 +538,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int k = 0; k < 32; k += 2) {
                         const int kk = cc * 32 + k;
-                        float p0 = fast_exp2(fmaf(__uint_as_float(cb[cc & 1][k]), c, nm));
-                        float p1 = fast_exp2(fmaf(__uint_as_float(cb[cc & 1][k + 1]), c, nm));
+                        const uint64_t arg =
+                            ffma2(f2(__uint_as_float(cb[cc & 1][k]), __uint_as_float(cb[cc & 1][k + 1])), c2, nm2);
+                        float p0, p1;
+                        if (((k >> 1) & 3) == 3) {               // one pair in four on the FMA pipe
+                            f2_split(exp2_poly2(arg), p0, p1);
+                        } else {
+                            float a0, a1;
+                            f2_split(arg, a0, a1);
+                            p0 = fast_exp2(a0);
+                            p1 = fast_exp2(a1);
+                        }
                         if constexpr (!kEasy) {
                             p0 = visible(kk) ? p0 : 0.f;
                             p1 = visible(kk + 1) ? p1 : 0.f;
                         }
                         const uint32_t w = pack_bf16x2(p0, p1);
                         packed[k / 2] = w;
-                        ls[(k / 2) & 3] += bf16_lo(w) + bf16_hi(w);
+                        lacc[(k >> 1) & 1] = fadd2(lacc[(k >> 1) & 1], f2(bf16_lo(w), bf16_hi(w)));
                     }
                     tmem_st16(s_col + cc * 16, packed);   // keys 32cc .. 32cc+31 of this row
                     if (cc < 3) tmemw::wait_ld(cb[(cc + 1) & 1]);
@@ -476,7 +563,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             };
             if (easy) emit(std::true_type{});
             else emit(std::false_type{});
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            {
+                float a0, a1, b0, b1;
+                f2_split(lacc[0], a0, a1);
+                f2_split(lacc[1], b0, b1);
+                l_run += (a0 + a1) + (b0 + b1);
+            }
             // V rows of keys outside the sequence or behind a bad table entry
             // may hold stale or non-finite bits; the MMA multiplies them by 0,
             // so zero them (thread <-> key row) once V has landed.  The group
