@@ -175,3 +175,19 @@ def test_copy_blocks_bitwise_on_gpu():
     pk.copy_blocks(t["k_cache"], t["v_cache"], t["copy_pairs"])
     kr, vr = oracle.copy_blocks(kb, vb, w.copy_pairs.tolist())
     assert np.array_equal(host_bits(t["k_cache"]), kr) and np.array_equal(host_bits(t["v_cache"]), vr)
+
+
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
+@pytest.mark.parametrize("scale", [0.0, -0.09, 0.3])
+def test_any_finite_scale(decode_path, scale):
+    # The scale multiplies q.k before the softmax whatever its sign: 0 gives
+    # the plain mean of V over the context, a negative scale favours the
+    # keys least aligned with q.
+    w = W.custom(23, [1, 16, 130, 600, 1500], 32, 8, 128, 16)
+    t = W.make_tensors(w, DEV)
+    out = pk.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"],
+                                    scale, w.block_size, out_dtype=torch.float32, max_seq_len=w.max_seq_len)
+    ref = oracle.paged_decode_attention(host_bits(t["q"]), host_bits(t["k_cache"]), host_bits(t["v_cache"]),
+                                        w.block_tables, w.seq_lens, scale, w.block_size)
+    assert_close(out.cpu().numpy(), ref, False, f"{decode_path} scale={scale}")
+    assert pk.pk_get_device_error() == 0

@@ -99,3 +99,41 @@ def test_wide_block_bf16_out_with_garbage_table_padding():
     out = _run(w, t, q, cu, 512, torch.bfloat16)
     assert_close(out.float().cpu().numpy(), _ref(w, t, q, cu), True, "wide bf16")
     assert pk.pk_get_device_error() == 0
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.09])
+@pytest.mark.parametrize("qmax", [2, 200])
+def test_multi_query_any_finite_scale(scale, qmax):
+    # Zero and negative scales on both kernels (narrow: 2 tokens x G = 8;
+    # wide: prompt chunks): the prefill softmax takes the row MIN of the raw
+    # scores when the scale is negative.
+    lens = [5, 130, 700, 1111]
+    qlens = [min(L, qmax) for L in lens]
+    w, t, q, cu = _case(29, lens, qlens, 8, 2, 128, 16)
+    out = pk.paged_attention_multi_query(q, torch.from_numpy(cu).to(DEV), max(qlens), t["k_cache"], t["v_cache"],
+                                         t["block_tables"], t["seq_lens"], scale, out_dtype=torch.float32,
+                                         max_seq_len=w.max_seq_len)
+    ref = oracle.paged_multi_query_attention(host_bits(q), host_bits(t["k_cache"]), host_bits(t["v_cache"]),
+                                             w.block_tables, w.seq_lens, cu.tolist(), scale, w.block_size)
+    assert_close(out.cpu().numpy(), ref, False, f"scale={scale} q={qmax}")
+    assert pk.pk_get_device_error() == 0
+
+
+def test_output_not_16_byte_aligned_is_refused_before_any_launch():
+    # Device pointers must be 16-byte aligned (the TMA store and the vector
+    # stores rely on it): a bf16 output 2 bytes into an allocation is
+    # refused on the host and left untouched.
+    lens = [300, 700]
+    qlens = [256, 300]
+    w, t, q, cu = _case(31, lens, qlens, 8, 2, 128, 16)
+    n = q.numel()
+    buf = torch.full((n + 8,), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[1:1 + n].view(q.shape)
+    assert out.data_ptr() % 16 != 0
+    with pytest.raises(pk.PagedKVError, match="ALIGNMENT"):
+        pk.paged_attention_multi_query(q, torch.from_numpy(cu).to(DEV), max(qlens), t["k_cache"], t["v_cache"],
+                                       t["block_tables"], t["seq_lens"], w.scale, out=out,
+                                       max_seq_len=w.max_seq_len)
+    torch.cuda.synchronize()
+    assert (buf.float().cpu().numpy() == 7.0).all()
+    assert pk.pk_get_device_error() == 0
