@@ -85,9 +85,12 @@ struct Misc {
     uint64_t o_full[2];       // P.V of a tile complete (per tile parity)
     uint64_t o_free[2];       // a segment's O buffer has been read out
     uint64_t drain;
-    int64_t scan[kThreads / 32 + 1];   // warp totals of the prologue scan
+    int64_t scan[kThreads / 32 + 1];   // warp totals of the prologue scans (tiles)
+    int64_t scan_w[kThreads / 32 + 1]; // (costs)
+    int64_t bnd[2];                    // first tile of this CTA's range and of the next one
     int64_t rem0;
     int32_t s0;
+    int32_t first_cta;                 // the CTA in whose range this CTA's first segment starts
     uint32_t tmem_base;
     int abort;
     int never;
@@ -103,10 +106,12 @@ constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 2 * kPBytes + sizeo
 // Workspace slot of a cut segment.
 struct Slot {
     int32_t flag;          // slot 0 only: 1 = this CTA merges the segment
-    int32_t s, h, pad;
+    int32_t s, h;
+    int32_t first_cta;     // slot 0 only: the CTA in whose range the segment starts
     int64_t start_tile;    // flattened index of the segment's (s, h) tile 0
     int64_t total_tiles;
-    int64_t pad2[4];
+    int64_t range_beg;     // slot 0 only: first tile of this CTA's range
+    int64_t pad2[3];
     float m[kNPad];
     float l[kNPad];
     float o[kNPad * 128];
@@ -137,7 +142,13 @@ struct Walk {
     }
 };
 
-__device__ __forceinline__ int64_t range_begin(int64_t c, int64_t T, int64_t C) { return c * T / C; }
+// The flattened (sequence, KV head, tile) space is cut into ranges of equal
+// cost, not of equal tile count: a CTA's time grows with the (sequence,
+// KV head) segments in its range (each loads its queries, sets up and reads
+// out its O) as well as with its tiles -- measured on the Llama-3-70B-shaped
+// batch, about 0.29 of a tile per segment.
+constexpr int64_t kTileCost = 7;
+constexpr int64_t kSegCost = 2;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -220,30 +231,80 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- this CTA's range of the flattened tile space ----------------------
+    // Tile x (its cost interval starting at a_x: a segment's tile 0 covers
+    // [start, start + kSegCost + kTileCost), tile t >= 1 starts at start +
+    // kSegCost + kTileCost * t) belongs to CTA k when P_k <= a_x < P_{k+1},
+    // P_k = k * W / C, W the total cost.
     const int per = (N + kThreads - 1) / kThreads;
     const int s_lo = min(N, static_cast<int>(threadIdx.x) * per), s_hi = min(N, s_lo + per);
-    int64_t mine = 0;
+    int64_t mine = 0, mine_w = 0;
     for (int s = s_lo; s < s_hi; ++s) {
         const int raw = p.seq_lens[s];
         if ((raw < 0 || raw > cap) && s % C == c) set_error(p.err, PK_DEVERR_SEQ_LEN);
         const int L = raw < 0 ? 0 : (raw > cap ? cap : raw);
-        mine += static_cast<int64_t>((L + kTile - 1) / kTile) * Hkv;
+        const int64_t nt = (L + kTile - 1) / kTile;
+        mine += nt * Hkv;
+        mine_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
     }
-    int64_t T;
+    int64_t T, W;
     const int64_t my_off = block_exclusive_scan<kThreads>(mine, misc->scan, &T);
-    const int64_t beg = range_begin(c, T, C), end = range_begin(c + 1, T, C);
+    const int64_t my_off_w = block_exclusive_scan<kThreads>(mine_w, misc->scan_w, &W);
+    for (int k = 0; k < 2; ++k) {
+        const int64_t P = static_cast<int64_t>(c + k) * W / C;
+        if (P >= W) {
+            if (threadIdx.x == 0) misc->bnd[k] = T;
+            continue;
+        }
+        if (my_off_w <= P && P < my_off_w + mine_w) {
+            int64_t acc_t = my_off, acc_w = my_off_w;
+            for (int s = s_lo; s < s_hi; ++s) {
+                const int64_t nt = (clamp_len(p, s, cap) + kTile - 1) / kTile;
+                const int64_t segc = kTileCost * nt + kSegCost;
+                const int64_t cw = nt > 0 ? segc * Hkv : 0;
+                if (P < acc_w + cw) {
+                    const int64_t q = P - acc_w;
+                    int64_t h = q / segc;
+                    const int64_t r = q - h * segc;
+                    // The first tile of the segment that starts at or after r.
+                    int64_t t = r == 0 ? 0 : (r - kSegCost + kTileCost - 1) / kTileCost;
+                    if (r > 0 && t < 1) t = 1;
+                    if (t >= nt) {
+                        ++h;
+                        t = 0;
+                    }
+                    misc->bnd[k] = acc_t + h * nt + t;
+                    break;
+                }
+                acc_t += nt * Hkv;
+                acc_w += cw;
+            }
+        }
+    }
+    __syncthreads();
+    const int64_t beg = misc->bnd[0], end = misc->bnd[1];
+    if (threadIdx.x == 0 && slots) slots[2 * c].range_beg = beg;
     const int n_tiles = static_cast<int>(end - beg);
     if (n_tiles > 0) {
-        int64_t acc = my_off;
+        int64_t acc = my_off, acc_w = my_off_w;
         if (acc <= beg && beg < acc + mine) {
             for (int s = s_lo; s < s_hi; ++s) {
-                const int64_t w = static_cast<int64_t>((clamp_len(p, s, cap) + kTile - 1) / kTile) * Hkv;
+                const int64_t nt = (clamp_len(p, s, cap) + kTile - 1) / kTile;
+                const int64_t w = nt * Hkv;
                 if (beg < acc + w) {
                     misc->s0 = s;
                     misc->rem0 = beg - acc;
+                    // If the range starts inside a segment, the CTA where that
+                    // segment starts (the owner of its tile 0's cost start).
+                    const int64_t h0 = (beg - acc) / nt;
+                    const int64_t a = acc_w + h0 * (kTileCost * nt + kSegCost);
+                    int64_t k = W > 0 ? a * C / W : 0;
+                    while (k + 1 < C && (k + 1) * W / C <= a) ++k;
+                    while (k > 0 && k * W / C > a) --k;
+                    misc->first_cta = static_cast<int32_t>(k);
                     break;
                 }
                 acc += w;
+                acc_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
             }
         }
     }
@@ -530,7 +591,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     sl->start_tile = beg + pend_i0 - pend_t0;
                     sl->total_tiles = T;
                     // Cut at its start and finished here: this CTA merges it.
-                    if (slot_idx == 0) sl->flag = (pend_t0 > 0 && pend_cut_end) ? 1 : 0;
+                    if (slot_idx == 0) {
+                        sl->flag = (pend_t0 > 0 && pend_cut_end) ? 1 : 0;
+                        sl->first_cta = misc->first_cta;
+                    }
                 }
             }
             pending = false;
@@ -723,6 +787,8 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
     const int flag = mine->flag;
     const int s = mine->s, h = mine->h;
     const int64_t start = mine->start_tile, T = mine->total_tiles;
+    const int ca = mine->first_cta;
+    const int64_t beg_prev = q0->range_beg;
     float mm[NC], ml[NC], mo[NC], am[NC], al[NC], ao[NC], bm[NC], bl[NC], bo[NC];
 #pragma unroll
     for (int g = 0; g < NC; ++g) {
@@ -737,12 +803,12 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
         bo[g] = q1->o[g * D + d];
     }
     if (flag != 1 || threadIdx.x >= D) return;
-    int ca = static_cast<int>(start * C / T);
-    while (ca + 1 < C && range_begin(ca + 1, T, C) <= start) ++ca;
+    // First tile of CTA cc's range (the decode grid wrote it into slot 0).
+    auto range_beg = [&](int cc) -> int64_t { return cc < C ? slots[2 * cc].range_beg : T; };
     float num[NC], den[NC];
     if (ca == c - 1) {
         // Two parts: CTA c - 1 (slot 0 if the segment is its first, else 1) and this CTA.
-        const bool first_of_prev = range_begin(c - 1, T, C) >= start;
+        const bool first_of_prev = beg_prev >= start;
 #pragma unroll
         for (int g = 0; g < NC; ++g) {
             const float pm = first_of_prev ? am[g] : bm[g];
@@ -761,16 +827,16 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
 #pragma unroll
         for (int g = 0; g < NC; ++g) M[g] = -INFINITY;
         for (int cc = ca; cc <= c; ++cc) {
-            if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
-            const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
+            if (range_beg(cc) == range_beg(cc + 1)) continue;
+            const Slot *sl = slots + 2 * cc + (range_beg(cc) >= start ? 0 : 1);
 #pragma unroll
             for (int g = 0; g < NC; ++g) M[g] = fmaxf(M[g], sl->m[g]);
         }
 #pragma unroll
         for (int g = 0; g < NC; ++g) num[g] = den[g] = 0.f;
         for (int cc = ca; cc <= c; ++cc) {
-            if (range_begin(cc, T, C) == range_begin(cc + 1, T, C)) continue;
-            const Slot *sl = slots + 2 * cc + (range_begin(cc, T, C) >= start ? 0 : 1);
+            if (range_beg(cc) == range_beg(cc + 1)) continue;
+            const Slot *sl = slots + 2 * cc + (range_beg(cc) >= start ? 0 : 1);
 #pragma unroll
             for (int g = 0; g < NC; ++g) {
                 const float a = rescale(sl->m[g], M[g]);
