@@ -420,9 +420,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 }
             }
             if (ok) {
+                if (B == 8) {
+                    // K of an 8-row page is one swizzle atom per half: one
+                    // box, [half][row][64] at the page's slot, like V.
+                    tma_load_5d(sbase + kKOff + r0 * 128 * NCH, &tm_k, full, 0, 0, 0, w.h, phys);
+                } else {
 #pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_4d(sbase + kKOff + ch * kChunkBytes + r0 * 128, &tm_k, full, ch * 64, w.h, 0, phys);
+                    for (int ch = 0; ch < NCH; ++ch)
+                        tma_load_4d(sbase + kKOff + ch * kChunkBytes + r0 * 128, &tm_k, full, ch * 64, w.h, 0, phys);
+                }
                 // V: one box per page, [half][row][64] at the page's slot.
                 tma_load_5d(sbase + kVOff + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, w.h, phys);
             }
@@ -470,9 +476,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const int sb = i & 1;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    // K rows: [half][128 rows][64] (atoms of 8 rows 1,024 bytes
+                    // apart), or for B = 8 page slots [half][8 rows][64] (atoms
+                    // v_page apart, the second half 1,024 bytes in).
+                    const uint32_t off = (kk >> 2) * (B == 8 ? 1024u : kChunkBytes) + (kk & 3) * 32;
                     const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
-                    const uint64_t a = smem_desc(sbase + kKOff + off, 16, 1024, kLayoutSw128);
+                    const uint64_t a = smem_desc(sbase + kKOff + off, 16, B == 8 ? v_page : 1024u, kLayoutSw128);
                     const uint64_t b = smem_desc(sbase + kQOff + qoff, 16, 1024, kLayoutSw128);
                     mma_bf16(tmem + kTmemS + sb * kNPad, a, b, kIdescQK, kk > 0 ? 1u : 0u);
                 }
@@ -984,7 +993,8 @@ size_t tc_workspace_bytes() { return 2 * kMaxCtas * sizeof(Slot); }
 
 cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream) {
     CUtensorMap mk, mv, mq;
-    if (!encode_cache_map(&mk, p.k_cache, p) || !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
+    if (!(p.block_size == 8 ? encode_value_map(&mk, p.k_cache, p) : encode_cache_map(&mk, p.k_cache, p)) ||
+        !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
         return cudaErrorInvalidValue;
     int C = sm_count();
     if (C <= 0) return cudaErrorNoDevice;
@@ -1008,7 +1018,8 @@ cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t s
 cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas) {
     CUtensorMap mk, mv, mq;
     if (ctas <= 0 || ctas > static_cast<int>(kMaxCtas)) return cudaErrorInvalidValue;
-    if (!encode_cache_map(&mk, p.k_cache, p) || !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
+    if (!(p.block_size == 8 ? encode_value_map(&mk, p.k_cache, p) : encode_cache_map(&mk, p.k_cache, p)) ||
+        !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
         return cudaErrorInvalidValue;
     return p.head_dim == 64 ? launch_d<64>(mk, mv, mq, p, ctas, stream) : launch_d<128>(mk, mv, mq, p, ctas, stream);
 }

@@ -318,7 +318,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     mbar_arrive_expect_tx(kfull, nok * B * 128u * NCH);
                 }
                 __syncwarp();
-                if (ok) {
+                if (ok && B == 8) {
+                    // K of an 8-row page is one swizzle atom per half: one
+                    // box, [half][row][64] at the page's slot, like V.
+                    tma_load_5d(base + kKOff + st * kKBytes + r0 * 128 * NCH, &tm_k, kfull, 0, 0, 0, h, phys);
+                } else if (ok) {
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch)
                         tma_load_4d(base + kKOff + st * kKBytes + ch * kChunk + r0 * 128, &tm_k, kfull, ch * 64, h, 0,
@@ -385,8 +389,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+                            // K: [half][128 keys][64], or for B = 8 page slots
+                            // [half][8 keys][64] (atoms v_page apart).
+                            const uint32_t koff = (kk >> 2) * (B == 8 ? 1024u : kChunk) + (kk & 3) * 32;
                             const uint64_t a = smem_desc(qbase + off, 16, 1024, kLayoutSw128);
-                            const uint64_t b = smem_desc(kbase + off, 16, 1024, kLayoutSw128);
+                            const uint64_t b = smem_desc(kbase + koff, 16, B == 8 ? v_page : 1024u, kLayoutSw128);
                             mma_bf16(s_col, a, b, kIdescS, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(smem_u32(&misc->s_full[x]));
@@ -721,7 +728,9 @@ cudaError_t launch_dg(const DecodeParams &p, int max_q_len, cudaStream_t stream)
     const cuuint64_t qstr[2] = {Dd * 2, Dd * p.num_heads * 2};
     const cuuint32_t qbox[3] = {64, G, kRows / G};
     CUtensorMap mk, mv, mq, mo;
-    if (!encode(&mk, p.k_cache, 4, cdims, cstr, cbox) || !encode(&mv, p.v_cache, 5, vdims, vstr, vbox) ||
+    const bool k_slots = B == 8;                  // K of 8-row pages: one box per page, like V
+    if (!(k_slots ? encode(&mk, p.k_cache, 5, vdims, vstr, vbox) : encode(&mk, p.k_cache, 4, cdims, cstr, cbox)) ||
+        !encode(&mv, p.v_cache, 5, vdims, vstr, vbox) ||
         !encode(&mq, p.q, 3, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
     // Full tiles of a bf16 output go out by TMA store; otherwise (fp32, or
