@@ -187,12 +187,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int N = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads, B = p.block_size;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * B);
     const int Gq = H / Hkv, lgG = __ffs(Gq) - 1;     // query heads per KV head (a power of two)
-    // V of a tile in shared memory: one slot of v_page bytes per page, each
-    // [half][row][64] (B is 8, 16 or 32).
-    const uint32_t v_page = static_cast<uint32_t>(B) * 128u * NCH;
-    const uint32_t v_half = static_cast<uint32_t>(B) * 128u;        // between the two 64-element halves
-    const uint32_t v_group = B >= 16 ? 1024u : v_page;              // between groups of 8 tokens
-    const int lgB = __ffs(B) - 1;                                    // B is a power of two
+    // K and V of a tile in shared memory: each page in one TMA box as B / 8
+    // blocks of 8 rows, each block [half][8 rows][64] -- so the 8-row
+    // swizzle atoms of one 64-element half lie kAtomStride bytes apart
+    // whatever the block size, a uniform stride for the MMA descriptors.
+    constexpr uint32_t kAtomStride = 1024u * NCH;
     constexpr bool mq = MQ;                           // several query tokens per sequence
     Slot *slots = static_cast<Slot *>(p.tc_slots);
 
@@ -420,17 +419,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 }
             }
             if (ok) {
-                if (B == 8) {
-                    // K of an 8-row page is one swizzle atom per half: one
-                    // box, [half][row][64] at the page's slot, like V.
-                    tma_load_5d(sbase + kKOff + r0 * 128 * NCH, &tm_k, full, 0, 0, 0, w.h, phys);
-                } else {
-#pragma unroll
-                    for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(sbase + kKOff + ch * kChunkBytes + r0 * 128, &tm_k, full, ch * 64, w.h, 0, phys);
-                }
-                // V: one box per page, [half][row][64] at the page's slot.
-                tma_load_5d(sbase + kVOff + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, w.h, phys);
+                // One box of K and one of V per page, at the page's place in the tile.
+                const int rb = phys * (B >> 3);                  // the page's first 8-row block
+                tma_load_5d(sbase + kKOff + r0 * 128 * NCH, &tm_k, full, 0, 0, 0, rb, w.h);
+                tma_load_5d(sbase + kVOff + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, rb, w.h);
             }
             ++issued;
             w.next(p, cap);
@@ -456,10 +448,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const uint32_t pbase = p_addr + pb * kPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
-                    // Tokens 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
-                    const uint32_t t0 = kk * 16;
-                    const uint64_t a = smem_desc(vbase + (t0 >> lgB) * v_page + (t0 & (B - 1)) * 128, v_half, v_group,
-                                                 kLayoutSw128);
+                    // Tokens 16kk .. 16kk+15: 8-row blocks 2kk and 2kk + 1; the
+                    // two 64-element halves 1,024 bytes apart.
+                    const uint64_t a = smem_desc(vbase + kk * 2 * kAtomStride, 1024, kAtomStride, kLayoutSw128);
                     const uint64_t b = smem_desc(pbase + kk * 512, 256, 128, kLayoutNone);
                     mma_bf16(tmem + kTmemO + (sg & 1) * kNPad, a, b, kIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
@@ -476,12 +467,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const int sb = i & 1;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    // K rows: [half][128 rows][64] (atoms of 8 rows 1,024 bytes
-                    // apart), or for B = 8 page slots [half][8 rows][64] (atoms
-                    // v_page apart, the second half 1,024 bytes in).
-                    const uint32_t off = (kk >> 2) * (B == 8 ? 1024u : kChunkBytes) + (kk & 3) * 32;
+                    // K: the half (kk / 4) of each 8-row block, 1,024 bytes in
+                    // for the second; atoms kAtomStride apart.
+                    const uint32_t off = (kk >> 2) * 1024u + (kk & 3) * 32;
                     const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
-                    const uint64_t a = smem_desc(sbase + kKOff + off, 16, B == 8 ? v_page : 1024u, kLayoutSw128);
+                    const uint64_t a = smem_desc(sbase + kKOff + off, 16, kAtomStride, kLayoutSw128);
                     const uint64_t b = smem_desc(sbase + kQOff + qoff, 16, 1024, kLayoutSw128);
                     mma_bf16(tmem + kTmemS + sb * kNPad, a, b, kIdescQK, kk > 0 ? 1u : 0u);
                 }
@@ -723,8 +713,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 // masked tokens may hold stale or non-finite bits, so zero them.
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
-                    uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + (row >> lgB) * v_page +
-                                                            ch * B * 128 + (row & (B - 1)) * 128);
+                    uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + st * kStageBytes + kVOff + (row >> 3) * kAtomStride +
+                                                            ch * 1024 + (row & 7) * 128);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
                 }
@@ -883,33 +873,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-// V pages: one box per (page, head) holding all B rows of both 64-element
-// halves, laid out [half][row][64] in shared memory (dimensions: 64
-// elements, row, half (128 bytes apart), head, page).
-bool encode_value_map(CUtensorMap *m, const void *base, const DecodeParams &p) {
+// K or V pages: one box per (page, KV head) holding its B rows as B / 8
+// blocks of 8 rows, each block [half][8 rows][64] in shared memory
+// (dimensions: 64 elements; row within the block; 64-element half, 128
+// bytes apart; 8-row block, numbered page * B / 8 + block; KV head).
+bool encode_page_map(CUtensorMap *m, const void *base, const DecodeParams &p) {
     auto enc = get_encoder();
     if (!enc) return false;
     const cuuint64_t D = p.head_dim, Hkv = p.num_kv_heads, B = p.block_size;
     const cuuint64_t P = p.num_blocks > 0 ? p.num_blocks : 1;
-    cuuint64_t dims[5] = {64, B, D / 64, Hkv, P};
-    cuuint64_t strides[4] = {Hkv * D * 2, 128, D * 2, B * Hkv * D * 2};
-    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(B), static_cast<cuuint32_t>(D / 64), 1, 1};
+    cuuint64_t dims[5] = {64, 8, D / 64, P * (B / 8), Hkv};
+    cuuint64_t strides[4] = {Hkv * D * 2, 128, 8 * Hkv * D * 2, D * 2};
+    cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(D / 64), static_cast<cuuint32_t>(B / 8), 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool encode_cache_map(CUtensorMap *m, const void *base, const DecodeParams &p) {
-    auto enc = get_encoder();
-    if (!enc) return false;
-    const cuuint64_t D = p.head_dim, Hkv = p.num_kv_heads, B = p.block_size;
-    const cuuint64_t P = p.num_blocks > 0 ? p.num_blocks : 1;
-    cuuint64_t dims[4] = {D, Hkv, B, P};
-    cuuint64_t strides[3] = {D * 2, Hkv * D * 2, B * Hkv * D * 2};
-    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(B), 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -993,8 +970,7 @@ size_t tc_workspace_bytes() { return 2 * kMaxCtas * sizeof(Slot); }
 
 cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream) {
     CUtensorMap mk, mv, mq;
-    if (!(p.block_size == 8 ? encode_value_map(&mk, p.k_cache, p) : encode_cache_map(&mk, p.k_cache, p)) ||
-        !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
+    if (!encode_page_map(&mk, p.k_cache, p) || !encode_page_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
         return cudaErrorInvalidValue;
     int C = sm_count();
     if (C <= 0) return cudaErrorNoDevice;
@@ -1018,8 +994,7 @@ cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t s
 cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas) {
     CUtensorMap mk, mv, mq;
     if (ctas <= 0 || ctas > static_cast<int>(kMaxCtas)) return cudaErrorInvalidValue;
-    if (!(p.block_size == 8 ? encode_value_map(&mk, p.k_cache, p) : encode_cache_map(&mk, p.k_cache, p)) ||
-        !encode_value_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
+    if (!encode_page_map(&mk, p.k_cache, p) || !encode_page_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
         return cudaErrorInvalidValue;
     return p.head_dim == 64 ? launch_d<64>(mk, mv, mq, p, ctas, stream) : launch_d<128>(mk, mv, mq, p, ctas, stream);
 }

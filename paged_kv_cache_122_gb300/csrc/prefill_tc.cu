@@ -186,12 +186,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int h = (blockIdx.x / qblocks) % Hkv;
     const int s = blockIdx.x / qblocks / Hkv;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * B);
-    // V of a key tile in shared memory: one slot of v_page bytes per page,
-    // each [half][row][64] (B is 8, 16 or 32).
-    const uint32_t v_page = static_cast<uint32_t>(B) * 128u * NCH;
-    const uint32_t v_half = static_cast<uint32_t>(B) * 128u;        // between the two 64-element halves
-    const uint32_t v_group = B >= 16 ? 1024u : v_page;              // between groups of 8 keys
-    const int lgB = __ffs(B) - 1;                                    // B is a power of two
+    // K and V of a key tile in shared memory: each page in one TMA box as
+    // B / 8 blocks of 8 rows, each block [half][8 rows][64] -- so the 8-row
+    // swizzle atoms of one 64-element half lie kAtomStride bytes apart
+    // whatever the block size.
+    constexpr uint32_t kAtomStride = 1024u * NCH;
     int L = p.seq_lens[s];
     const int q0 = p.cu_q_lens[s];
     const int qn = p.cu_q_lens[s + 1] - q0;
@@ -318,22 +317,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     mbar_arrive_expect_tx(kfull, nok * B * 128u * NCH);
                 }
                 __syncwarp();
-                if (ok && B == 8) {
-                    // K of an 8-row page is one swizzle atom per half: one
-                    // box, [half][row][64] at the page's slot, like V.
-                    tma_load_5d(base + kKOff + st * kKBytes + r0 * 128 * NCH, &tm_k, kfull, 0, 0, 0, h, phys);
-                } else if (ok) {
-#pragma unroll
-                    for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(base + kKOff + st * kKBytes + ch * kChunk + r0 * 128, &tm_k, kfull, ch * 64, h, 0,
-                                    phys);
-                }
+                // One box per page, at the page's place in the tile.
+                if (ok) tma_load_5d(base + kKOff + st * kKBytes + r0 * 128 * NCH, &tm_k, kfull, 0, 0, 0, phys * (B >> 3), h);
             } else {
                 const uint32_t vfull = smem_u32(&misc->vfull[st]);
                 if (lane == 0) mbar_arrive_expect_tx(vfull, nok * B * 128u * NCH);
                 __syncwarp();
-                // V: one box per page, [half][row][64] at the page's slot.
-                if (ok) tma_load_5d(base + kVOff + st * kVBytes + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, h, phys);
+                // One box per page, at the page's place in the tile.
+                if (ok) tma_load_5d(base + kVOff + st * kVBytes + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, phys * (B >> 3), h);
             }
             ++issued;
             if (i + 1 < nT) phys_next = fetch(i + 1);
@@ -370,10 +361,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         const uint32_t vbase = base + kVOff + (t % kVStages) * kVBytes;
 #pragma unroll
                         for (int kk = 0; kk < kKeys / 16; ++kk) {
-                            // Keys 16kk .. 16kk+15: page (16kk / B) at its slot, row 16kk % B.
-                            const uint32_t k0 = kk * 16;
-                            const uint64_t b = smem_desc(vbase + (k0 >> lgB) * v_page + (k0 & (B - 1)) * 128, v_half,
-                                                         v_group, kLayoutSw128);
+                            // Keys 16kk .. 16kk+15: 8-row blocks 2kk and 2kk + 1;
+                            // the two 64-element halves 1,024 bytes apart.
+                            const uint64_t b = smem_desc(vbase + kk * 2 * kAtomStride, 1024, kAtomStride, kLayoutSw128);
                             mma_bf16_tmem_a(tmem + kTmemO + x * 128, s_col + kk * 8, b, kIdescO,
                                             (t > 0 || kk > 0) ? 1u : 0u);
                         }
@@ -389,11 +379,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-                            // K: [half][128 keys][64], or for B = 8 page slots
-                            // [half][8 keys][64] (atoms v_page apart).
-                            const uint32_t koff = (kk >> 2) * (B == 8 ? 1024u : kChunk) + (kk & 3) * 32;
+                            // K: the half (kk / 4) of each 8-row block, 1,024
+                            // bytes in for the second; atoms kAtomStride apart.
+                            const uint32_t koff = (kk >> 2) * 1024u + (kk & 3) * 32;
                             const uint64_t a = smem_desc(qbase + off, 16, 1024, kLayoutSw128);
-                            const uint64_t b = smem_desc(kbase + koff, 16, B == 8 ? v_page : 1024u, kLayoutSw128);
+                            const uint64_t b = smem_desc(kbase + koff, 16, kAtomStride, kLayoutSw128);
                             mma_bf16(s_col, a, b, kIdescS, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(smem_u32(&misc->s_full[x]));
@@ -589,7 +579,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int ch = 0; ch < NCH; ++ch) {
                         uint4 *vrow = reinterpret_cast<uint4 *>(smem + kVOff + (i % kVStages) * kVBytes +
-                                                                (row >> lgB) * v_page + ch * B * 128 + (row & (B - 1)) * 128);
+                                                                (row >> 3) * kAtomStride + ch * 1024 + (row & 7) * 128);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
                     }
@@ -715,22 +705,19 @@ template <int D, int G>
 cudaError_t launch_dg(const DecodeParams &p, int max_q_len, cudaStream_t stream) {
     const cuuint64_t Dd = p.head_dim, Hkv = p.num_kv_heads, B = p.block_size;
     const cuuint64_t P = p.num_blocks > 0 ? p.num_blocks : 1;
-    const cuuint64_t cdims[4] = {Dd, Hkv, B, P};
-    const cuuint64_t cstr[3] = {Dd * 2, Hkv * Dd * 2, B * Hkv * Dd * 2};
-    const cuuint32_t cbox[4] = {64, 1, static_cast<cuuint32_t>(B), 1};
-    // V: one box per (page, head) with all B rows of both halves, [half][row][64].
-    const cuuint64_t vdims[5] = {64, B, Dd / 64, Hkv, P};
-    const cuuint64_t vstr[4] = {Hkv * Dd * 2, 128, Dd * 2, B * Hkv * Dd * 2};
-    const cuuint32_t vbox[5] = {64, static_cast<cuuint32_t>(B), static_cast<cuuint32_t>(Dd / 64), 1, 1};
+    // K and V: one box per (page, KV head) holding its B rows as B / 8 blocks
+    // of [half][8 rows][64] (dimensions: 64 elements; row within the block;
+    // half, 128 bytes apart; 8-row block, page * B / 8 + block; KV head).
+    const cuuint64_t pdims[5] = {64, 8, Dd / 64, P * (B / 8), Hkv};
+    const cuuint64_t pstr[4] = {Hkv * Dd * 2, 128, 8 * Hkv * Dd * 2, Dd * 2};
+    const cuuint32_t pbox[5] = {64, 8, static_cast<cuuint32_t>(Dd / 64), static_cast<cuuint32_t>(B / 8), 1};
     // Queries (and bf16 outputs) [total_q, H, D]: box (64 elements, G heads,
     // 128 / G tokens) = one query tile, row = token * G + head.
     const cuuint64_t qdims[3] = {Dd, static_cast<cuuint64_t>(p.num_heads), static_cast<cuuint64_t>(p.total_q)};
     const cuuint64_t qstr[2] = {Dd * 2, Dd * p.num_heads * 2};
     const cuuint32_t qbox[3] = {64, G, kRows / G};
     CUtensorMap mk, mv, mq, mo;
-    const bool k_slots = B == 8;                  // K of 8-row pages: one box per page, like V
-    if (!(k_slots ? encode(&mk, p.k_cache, 5, vdims, vstr, vbox) : encode(&mk, p.k_cache, 4, cdims, cstr, cbox)) ||
-        !encode(&mv, p.v_cache, 5, vdims, vstr, vbox) ||
+    if (!encode(&mk, p.k_cache, 5, pdims, pstr, pbox) || !encode(&mv, p.v_cache, 5, pdims, pstr, pbox) ||
         !encode(&mq, p.q, 3, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
     // Full tiles of a bf16 output go out by TMA store; otherwise (fp32, or
