@@ -150,11 +150,16 @@ struct Walk {
 constexpr int64_t kTileCost = 7;
 constexpr int64_t kSegCost = 2;
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+// Warp max of a float in one integer reduction: the bits are mapped to an
+// unsigned key with the same order (a non-negative float gets its sign bit
+// set, a negative one all bits flipped), reduced, and mapped back.
+__device__ __forceinline__ float warp_max_redux(float v) {
+    const uint32_t b = __float_as_uint(v);
+    const uint32_t key = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+    return __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
 }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -641,7 +646,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 // Rare: move the reference to the running max.
 #pragma unroll
                 for (int g = 0; g < NC; ++g) {
-                    const float mx = warp_max(s2[g]);
+                    const float mx = warp_max_redux(s2[g]);
                     if (lane == 0) misc->red[quad][g] = mx;
                 }
                 named_bar_sync(1, 128);
