@@ -9,17 +9,19 @@
 // its reduce step).
 //
 // Work split.  The flattened space (sequence, KV head, 128-token tile) is cut
-// into gridDim.x equal contiguous ranges, one per persistent CTA (one CTA per
-// SM).  A CTA's range covers whole (sequence, head) segments, which it writes
-// straight to the output, plus at most two cut segments at its ends, whose
-// partial (max, denominator, unnormalised output) go to a workspace slot and
-// are combined by the merge kernel.
+// into gridDim.x contiguous ranges of equal cost (a tile costs kTileCost, a
+// (sequence, head) segment kSegCost more), one per persistent CTA (one CTA
+// per SM).  A CTA's range covers whole segments, which it writes straight to
+// the output, plus at most two cut segments at its ends, whose partial (max,
+// denominator, unnormalised output) go to a workspace slot and are combined
+// by the merge kernel.
 //
 // Per 128-token tile, inside a CTA (192 threads):
 //   warp 0  producer: reads the tile's block-table entries one tile ahead
 //           (one lane per page), checks them, and TMA-loads each page's K rows
-//           and then V rows of this KV head (two 128-byte-swizzled 64-column
-//           boxes each) into a 3-stage shared-memory ring; K (with the
+//           and then V rows of this KV head (one box each, landing as 8-row
+//           blocks [half][8 rows][64] with the 128-byte swizzle) into a
+//           3-stage shared-memory ring; K (with the
 //           group's 16 query rows, loaded only when the stage does not hold
 //           them already) and V complete separate barriers, so the scores
 //           can start while V is still landing; the tile's position

@@ -27,9 +27,10 @@
 //
 // Per CTA (352 threads):
 //   warp 0     producer: both Q tiles once, then per key tile the K rows
-//              of each page (two 64-element halves) into a K ring;
-//   warp 10    producer: per key tile the V rows of each page (one box)
-//              into a V ring;
+//              of each page (one box: 8-row blocks [half][8 rows][64])
+//              into a K ring;
+//   warp 10    producer: per key tile the V rows of each page (one box,
+//              likewise) into a V ring;
 //   warp 1     MMA issuer (one thread): per key tile i, P.V(i-1) then S(i)
 //              for tile 0, then the same for tile 1;
 //   warps 2-5  softmax of tile 0, warps 6-9 softmax of tile 1: row max
