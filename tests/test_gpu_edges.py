@@ -62,6 +62,19 @@ def test_group_and_head_dim(G, D, decode_path):
 
 
 @pytest.mark.parametrize("decode_path", PATHS, indirect=True)
+@pytest.mark.parametrize("G,B", [(4, 8), (8, 8), (4, 32), (8, 32)])
+def test_head_dim_64_with_small_and_large_blocks(G, B, decode_path):
+    # A 64-element head is one swizzle half: each page lands as B / 8 blocks
+    # of [8 rows][64], for the blocks sizes other than the default too.
+    Hkv = 2
+    w = W.custom(6, [1, 9, 130, 700, 1500], G * Hkv, Hkv, 64, B)
+    t = W.make_tensors(w, DEV)
+    out = _attend(w, t)
+    assert_close(out.cpu().numpy(), _ref(w, t), False, f"G={G} D=64 B={B}")
+    assert pk.pk_get_device_error() == 0
+
+
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
 def test_physical_relabelling_gives_identical_bits(decode_path):
     w = W.custom(5, [3, 300, 1000, 2500], 32, 8, 128, 16)
     t = W.make_tensors(w, DEV)

@@ -72,7 +72,7 @@ def test_one_query_per_sequence_equals_decode_bit_for_bit():
 
 
 @pytest.mark.parametrize("G,qmax", [(8, 3), (8, 64), (4, 100), (1, 300), (16, 40), (2, 129)])
-@pytest.mark.parametrize("D,B", [(128, 16), (64, 32), (128, 8)])
+@pytest.mark.parametrize("D,B", [(128, 16), (64, 32), (128, 8), (64, 8)])
 def test_wide_query_blocks_match_oracle(G, qmax, D, B):
     # Prompt chunks: 128 / G query tokens x G heads per CTA over the key tiles.
     Hkv = 2
