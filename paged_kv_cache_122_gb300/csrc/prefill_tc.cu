@@ -82,6 +82,7 @@ struct Misc {
     uint64_t s_full[2];         // S of query tile X in TMEM
     uint64_t p_full[2];         // P of query tile X written (4 softmax warps)
     uint64_t pv_done[2];        // P.V of query tile X done
+    uint64_t go;                // tile 0's group has finished key tile 0 (4 warps)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -229,6 +230,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             mbar_init(smem_u32(&misc->p_full[x]), 4);
             mbar_init(smem_u32(&misc->pv_done[x]), 1);
         }
+        mbar_init(smem_u32(&misc->go), 4);
         mbar_init(smem_u32(&misc->drain), 1);
         misc->abort = 0;
         misc->never = 0;
@@ -424,10 +426,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 break;
             }
             // Tile 1's group starts half a period behind tile 0's (it
-            // begins key tile 0 once tile 0 has finished it), so that the
-            // MMAs of one group run while the other computes.
+            // begins key tile 0 once tile 0's group has finished it), so that
+            // the MMAs of one group run while the other computes.  (A barrier
+            // of its own: p_full[0] may have moved on by more than a phase.)
             if (x == 1 && i == 0 && n0 > 0 &&
-                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->p_full[0]), 0, &misc->abort, kWaitLimitNs))) {
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->go), 0, &misc->abort, kWaitLimitNs))) {
                 alive = false;
                 break;
             }
@@ -591,6 +594,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&misc->p_full[x]));
+            if (x == 0 && i == 0 && lane == 0) mbar_arrive(smem_u32(&misc->go));
         }
         if (alive && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->pv_done[x]), (nx - 1) & 1, &misc->abort,
                                                          kWaitLimitNs)))
