@@ -51,7 +51,7 @@ DOMINANT_SOURCES = ["paged_kv_cache_122_gb300/csrc/decode_tc.cu", "paged_kv_cach
                     "paged_kv_cache_122_gb300/csrc/block_scan.cuh"]
 # DRAM bytes per launch of the dominant kernel from one ncu capture, and the
 # hash of its sources at that time (profiles/ holds the summary).
-RECORDED_TRAFFIC = {"sources_sha1": "a8ace36aa4e10207bc375f008748c22ff304b1fe", "bytes_per_launch": 1125137664, "workload": "l3-70b"}
+RECORDED_TRAFFIC = {"sources_sha1": "b6672b3a452ea41edf629f4c2105788473c27266", "bytes_per_launch": 1125137664, "workload": "l3-70b"}
 
 
 def sources_sha1() -> str:
@@ -558,7 +558,9 @@ def run_ours(args):
     # Launches of this library per step: copy, append, then the decode kernel
     # and its merge (the merge runs when a sequence can span several CTAs /
     # partitions: > 128 tokens on tensor cores, > 512 on CUDA cores).
-    tensor_core = args.decode_path.startswith("tensor_core") or (args.decode_path == "auto" and w.group >= 4)
+    max_tiles = w.num_seqs * w.num_kv_heads * ((w.max_seq_len + 127) // 128)
+    tensor_core = args.decode_path.startswith("tensor_core") or \
+        (args.decode_path == "auto" and max_tiles >= torch.cuda.get_device_properties(dev).multi_processor_count)
     head_batched = args.decode_path == "tensor_core_head_batched" and w.num_kv_heads == 8 and \
         w.block_size in (16, 32) and w.group <= 8
     merge = (not head_batched) and w.max_seq_len > (128 if tensor_core else 512)   # fused when head-batched
@@ -833,7 +835,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-seqs", type=int, default=32)
     ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core", "tensor_core_head_batched"],
-                    help="kernel family of paged_attention_decode (auto: tensor cores for G >= 4)")
+                    help="kernel family of paged_attention_decode (auto: tensor cores)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     if args.prefill_only:

@@ -220,8 +220,9 @@ int pk_paged_attention_multi_query(void *out, int out_dtype, const void *q, int 
 
 /* Kernel family of pk_paged_attention_decode, process-wide. */
 enum pk_decode_path {
-    PK_PATH_AUTO = 0,                    /* tensor cores (per-head tiles) when G >= 4,
-                                            CUDA cores otherwise */
+    PK_PATH_AUTO = 0,                    /* tensor cores (per-head tiles) for every
+                                            group size, CUDA cores for a batch too
+                                            small to give each SM one 128-token tile */
     PK_PATH_CUDA_CORE = 1,               /* fp32 FMA on CUDA cores, one CTA per partition */
     PK_PATH_TENSOR_CORE = 2,             /* tcgen05 MMA, persistent CTAs, tiles of
                                             128 tokens x 1 KV head */

@@ -13,10 +13,13 @@ bool group_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G =
 // Partition size of the CUDA-core path.
 constexpr int kCudaCorePartTokens = 512;
 
-// Smallest group for which the automatic choice uses the tensor cores: from
-// G = 4 on, the scores of a 128-token tile are a [128 x D] x [D x G]
-// contraction and fp32 FMA issue, not HBM, would bound the CUDA-core kernel.
-constexpr int kTensorCoreMinGroup = 4;
+// Smallest group for which the automatic choice uses the tensor cores: all of
+// them.  From G = 4 on, the scores of a 128-token tile are a [128 x D] x
+// [D x G] contraction and fp32 FMA issue, not HBM, would bound the CUDA-core
+// kernel; at G = 1 and 2 the tensor-core kernel still streams the pages
+// faster (measured on a Llama-3-70B length mix with 8 KV heads, D = 128:
+// 6.2 against 4.3 TB/s at G = 1, 6.2 against 4.1 at G = 2; equal at D = 64).
+constexpr int kTensorCoreMinGroup = 1;
 
 std::atomic<int> g_path{PK_PATH_AUTO};
 
@@ -90,9 +93,15 @@ extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q
     p.scale_log2 = scale * pk::kLog2e;
     const int path = g_path.load();
     const int G = num_heads / num_kv_heads;
+    // A batch whose 128-token tiles could not give every SM even one (at most
+    // num_seqs * Hkv * ceil(max_seq_len / 128) of them) is bound by launch
+    // latency, where the CUDA-core kernel, without the persistent kernel's
+    // set-up, answers sooner (4 short sequences: ~15 against ~18 us).
+    const int64_t max_tiles = static_cast<int64_t>(num_seqs) * num_kv_heads * ceil_div(max_seq_len, 128);
+    const bool tiny = max_tiles < pk::sm_count();
     const bool tensor_core = max_seq_len > 0 &&
         (path == PK_PATH_TENSOR_CORE || path == PK_PATH_TENSOR_CORE_HEAD_BATCHED ||
-         (path == PK_PATH_AUTO && G >= kTensorCoreMinGroup));
+         (path == PK_PATH_AUTO && G >= kTensorCoreMinGroup && !tiny));
     const bool head_batched = path == PK_PATH_TENSOR_CORE_HEAD_BATCHED && tensor_core &&
                               pk::hb_supported(num_heads, num_kv_heads, head_dim, block_size);
     if (tensor_core) {
