@@ -1,7 +1,7 @@
-// Wide tensor-memory moves for kernels whose threads own a whole row of a
-// 128-lane accumulator: 64 consecutive 32-bit columns per instruction, with
-// the completion wait split from the load so that several loads can be in
-// flight before the thread blocks.
+// Wide tensor-memory loads for kernels whose threads own a whole row of a
+// 128-lane accumulator: 32 or 64 consecutive 32-bit columns per instruction,
+// with the completion wait split from the load so that several loads can be
+// in flight before the thread blocks.
 #pragma once
 
 #include <cstdint>
@@ -58,30 +58,6 @@ __device__ __forceinline__ void wait_ld(uint32_t (&r)[N]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-// Store 64 columns of this thread's lane (32x32b.x64); completion is awaited
-// with tcgen05.wait::st.
-__device__ __forceinline__ void st64(uint32_t taddr, const uint32_t (&v)[64]) {
-    __syncwarp();
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], "
-        "{"
-        "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
-        "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
-        "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64"
-        "};"
-        ::"r"(taddr),
-          "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-          "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
-          "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]),
-          "r"(v[32]), "r"(v[33]), "r"(v[34]), "r"(v[35]), "r"(v[36]), "r"(v[37]), "r"(v[38]), "r"(v[39]),
-          "r"(v[40]), "r"(v[41]), "r"(v[42]), "r"(v[43]), "r"(v[44]), "r"(v[45]), "r"(v[46]), "r"(v[47]),
-          "r"(v[48]), "r"(v[49]), "r"(v[50]), "r"(v[51]), "r"(v[52]), "r"(v[53]), "r"(v[54]), "r"(v[55]),
-          "r"(v[56]), "r"(v[57]), "r"(v[58]), "r"(v[59]), "r"(v[60]), "r"(v[61]), "r"(v[62]), "r"(v[63])
-        : "memory");
 }
 
 }  // namespace tmemw
