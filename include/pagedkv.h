@@ -205,9 +205,9 @@ int pk_paged_attention_decode_noalloc(void *out, int out_dtype, const void *q,
  * Tensor cores.  Narrow blocks (G * q <= 16 with q = max_q_len rounded up
  * to a power of two: e.g. G = 8, 2 tokens; speculative verification) use
  * one MMA column per (query token, query head) in the decode kernel; wider
- * blocks (prompt chunks) use a kernel with 128 query rows (128 / G tokens x
- * G heads) per CTA over the sequence's key tiles; the workspace is then not
- * used.  A sequence with more queries than tokens sets PK_DEVERR_SEQ_LEN
+ * blocks (prompt chunks) use a kernel whose CTAs each take two query tiles
+ * of 128 rows (128 / G tokens x G heads each) of one sequence and KV head
+ * over the sequence's key tiles; the workspace is then not used.  A sequence with more queries than tokens sets PK_DEVERR_SEQ_LEN
  * (its rows are then unspecified).
  */
 int pk_paged_attention_multi_query(void *out, int out_dtype, const void *q, int total_q,
