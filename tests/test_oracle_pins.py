@@ -92,6 +92,21 @@ def test_byte_counts_printed_on_pages():
         assert c["num_seqs"] * ref.num_logical_blocks(c["max_model_len"], c["block_size"]) == c["numel"]
 
 
+def test_block_table_has_room_for_a_ragged_longest_sequence():
+    # "PagedAttention from First Principles" §6: a row holds one entry per block
+    # of the longest allowed sequence, the last block partly filled included.
+    assert ref.block_table_bytes(1, 17, 16) == 8          # 17 tokens: 2 blocks of 16
+    assert ref.block_table_bytes(2, 1, 16) == 8           # 1 token: 1 block per sequence
+    assert ref.block_table_bytes(200, 8193, 16) == 410_400  # 513 entries of 4 bytes
+    # A row of that many entries is exactly long enough for the gather.
+    cache = np.zeros((4, 16, 1, 2), dtype=np.uint16)
+    row = [3, 1]
+    assert len(row) * 4 == ref.block_table_bytes(1, 17, 16)
+    assert ref.gather_sequence(cache, row, 17, 16, 0).shape == (17, 2)
+    with pytest.raises(ValueError):
+        ref.gather_sequence(cache, row[:1], 17, 16, 0)
+
+
 # ---------------------------------------------------------------------------
 # Block manager: copy-on-write and sharing examples
 # ---------------------------------------------------------------------------
@@ -173,6 +188,27 @@ def test_block_manager_rejects_partial_prefix_share_and_runs_dry():
         bm.append_slot("a")
     with pytest.raises(MemoryError):
         bm.append_slot("a")
+
+
+def test_freed_blocks_join_the_back_of_the_free_list():
+    # "How vLLM and PagedAttention Actually Work" §6 (Python blueprint): a new
+    # block is the front id of the free list, and a block whose count drops to
+    # zero is appended to the list.  Pool of 4 blocks of 2 tokens, worked by hand:
+    # a -> 0, b -> 1; freeing a leaves [2, 3, 0]; then c -> 2, d -> 3, e -> 0.
+    bm = oracle.CowBlockManager(4, 2)
+    for seq in ("a", "b"):
+        bm.new_sequence(seq)
+        for _ in range(2):
+            bm.append_slot(seq)
+    bm.free_sequence("a")
+    assert bm.free == [2, 3, 0]
+    for seq in ("c", "d", "e"):
+        bm.new_sequence(seq)
+        bm.append_slot(seq)
+    assert (bm.tables["c"], bm.tables["d"], bm.tables["e"]) == ([2], [3], [0])
+    with pytest.raises(MemoryError):
+        bm.new_sequence("f")
+        bm.append_slot("f")
 
 
 # ---------------------------------------------------------------------------
