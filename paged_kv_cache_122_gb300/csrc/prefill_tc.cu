@@ -135,40 +135,6 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
     return r;
 }
 
-// 2^x of a pair on the FMA pipe (the softmax gives a share of its
-// exponentials to it, the rest to the SFU).  x = n + f with n = floor(x) --
-// adding 1.5 * 2^23 rounded toward -inf leaves n in the low mantissa bits --
-// and f in [0, 1); 2^f is a cubic, 2^n is added to the exponent field.  The
-// cubic's coefficients are the minimax fit of 2^f on [0, 1) for relative
-// error (solved as a linear programme over 4,096 points): relative error
-// below 7.5e-5 (1.1e-4 with fp32 evaluation), far under the bf16 rounding
-// the weights get next.  x is clamped to -126 first, so that the exponent
-// field cannot wrap (a weight below 2^-126 is 0 to bf16 precision in a sum
-// of weights near 1).
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x) {
-    constexpr float kMagic = 12582912.0f;                   // 1.5 * 2^23
-    constexpr float kC0 = 0.99992520f, kC1 = 0.69583356f, kC2 = 0.22606714f, kC3 = 0.07802454f;
-    float xl, xh;
-    f2_split(x, xl, xh);
-    asm("max.NaN.f32 %0, %0, 0fC2FC0000;" : "+f"(xl));     // max(x, -126), NaN stays NaN
-    asm("max.NaN.f32 %0, %0, 0fC2FC0000;" : "+f"(xh));
-    x = f2(xl, xh);
-    const uint64_t m2 = f2(kMagic, kMagic);
-    uint64_t t, n, fr;
-    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(t) : "l"(x), "l"(m2));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(n) : "l"(t), "l"(m2));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(fr) : "l"(x), "l"(n));
-    uint64_t pp = ffma2(f2(kC3, kC3), fr, f2(kC2, kC2));
-    pp = ffma2(pp, fr, f2(kC1, kC1));
-    pp = ffma2(pp, fr, f2(kC0, kC0));
-    float pl, ph, tl, th;
-    f2_split(pp, pl, ph);
-    f2_split(t, tl, th);
-    // t's bits are those of 1.5 * 2^23 plus n; shifted by 23 only n << 23 remains.
-    return f2(__uint_as_float(__float_as_uint(pl) + (__float_as_uint(tl) << 23)),
-              __uint_as_float(__float_as_uint(ph) + (__float_as_uint(th) << 23)));
-}
-
 // grid: one CTA per (sequence, KV head, pair of query tiles of 128 / G
 // tokens each), blockIdx.x = (s * Hkv + h) * qblocks + j; CTAs past a
 // sequence's queries exit.  tm_o (bf16 output only, o_tma != 0) stores
@@ -536,15 +502,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         const int kk = cc * 32 + k;
                         const uint64_t arg =
                             ffma2(f2(__uint_as_float(cb[cc & 1][k]), __uint_as_float(cb[cc & 1][k + 1])), c2, nm2);
-                        float p0, p1;
-                        if (((k >> 1) & 3) == 3) {               // one pair in four on the FMA pipe
-                            f2_split(exp2_poly2(arg), p0, p1);
-                        } else {
-                            float a0, a1;
-                            f2_split(arg, a0, a1);
-                            p0 = fast_exp2(a0);
-                            p1 = fast_exp2(a1);
-                        }
+                        float a0, a1;
+                        f2_split(arg, a0, a1);
+                        float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
                         if constexpr (!kEasy) {
                             p0 = visible(kk) ? p0 : 0.f;
                             p1 = visible(kk + 1) ? p1 : 0.f;
