@@ -216,6 +216,79 @@ print(json.dumps(out))
 """
 
 
+# All host cores: the same oracle over the same sample, one sequence per work
+# item, in a pool of single-threaded worker processes started with spawn (the
+# subprocess that owns the pool never touches the GPU).  The sample's arrays are
+# written once to a temporary folder and memory-mapped by every worker.
+POOL_SNIPPET = r"""
+import json, os, sys, time, tempfile, shutil
+sys.path.insert(0, {root!r})
+import numpy as np
+import multiprocessing as mp
+import bench
+from paged_kv_cache_122_gb300 import workloads as W, metrics as M
+w = W.get({workload!r}, {seed})
+sel = list(range(min({nseq}, w.num_seqs)))
+wc = W.custom({seed}, w.seq_lens[sel], w.num_heads, w.num_kv_heads, w.head_dim, w.block_size)
+t = W.make_tensors(wc, "cpu")
+folder = tempfile.mkdtemp(prefix="pk_oracle_pool_")
+try:
+    for name, arr in (("q", W.bits(t["q"])), ("k", W.bits(t["k_cache"])), ("v", W.bits(t["v_cache"])),
+                      ("bt", np.asarray(wc.block_tables)), ("lens", np.asarray(wc.seq_lens))):
+        np.save(os.path.join(folder, name + ".npy"), arr)
+    del t
+    cores = len(os.sched_getaffinity(0))
+    order = sorted(range(len(sel)), key=lambda s: -int(wc.seq_lens[s]))     # longest first
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=bench._pool_init,
+                  initargs=(folder, float(wc.scale), int(wc.block_size))) as pool:
+        list(pool.imap_unordered(bench._pool_task, order))                   # warm-up pass
+        times = []
+        t_end = time.perf_counter() + {budget}
+        while True:
+            t0 = time.perf_counter()
+            list(pool.imap_unordered(bench._pool_task, order))
+            times.append(time.perf_counter() - t0)
+            if time.perf_counter() > t_end or len(times) >= 1000:
+                break
+finally:
+    shutil.rmtree(folder, ignore_errors=True)
+print(json.dumps({{"times": times, "bytes": M.useful_bytes(wc)["attention"], "seqs": len(sel),
+                  "tokens": int(wc.seq_lens.sum()), "cores": cores}}))
+"""
+
+_POOL = None
+
+
+def _pool_init(folder, scale, block_size):
+    """Worker start-up of the all-cores oracle pass: map the sample's arrays."""
+    global _POOL
+    import numpy as np
+
+    def ld(name, mode=None):
+        return np.load(os.path.join(folder, name + ".npy"), mmap_mode=mode)
+    _POOL = (ld("q"), ld("k", "r"), ld("v", "r"), ld("bt"), ld("lens"), scale, block_size)
+
+
+def _pool_task(s):
+    """One work item of the all-cores oracle pass: sequence ``s``."""
+    import oracle
+    q, kc, vc, bt, lens, scale, block_size = _POOL
+    oracle.paged_decode_attention(q[s:s + 1], kc, vc, bt[s:s + 1], lens[s:s + 1], scale, block_size)
+    return s
+
+
+def run_cpu_oracle_pool(workload: str, seed: int, nseq: int, budget_s: float, timeout_s: float = 240.0):
+    """The oracle over the sample on every host core (one process per core)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = POOL_SNIPPET.format(root=ROOT, workload=workload, seed=seed, nseq=nseq, budget=budget_s)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=timeout_s)
+    if res.returncode != 0:
+        raise RuntimeError(f"all-cores oracle run failed:\n{res.stderr[-2000:]}")
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
 def run_block_manager(workload: str, seed: int, steps: int, with_oracle: bool):
     """Host block-manager time of one decode step (append every sequence, take
     the copy pairs, export tables and lengths), on one pinned host core."""
@@ -776,6 +849,19 @@ def run_ours(args):
                       f"({r['tokens']} tokens) of the same workload, {len(r['times'])} passes, "
                       f"{tot:.1f} s on one pinned host core",
         }
+        if args.cpu_all_cores_budget > 0:
+            try:
+                rp = run_cpu_oracle_pool(args.workload, args.seed, args.cpu_seqs, args.cpu_all_cores_budget)
+                totp = sum(rp["times"])
+                res["cpu_baseline"]["all_cores"] = {
+                    "value": round(rp["bytes"] * len(rp["times"]) / totp / 1e9, 4),
+                    "unit": "GB/s",
+                    "cores": rp["cores"],
+                    "sample": f"the same {rp['seqs']} sequences, one sequence per work item on a pool of "
+                              f"{rp['cores']} single-threaded processes, {len(rp['times'])} passes, {totp:.1f} s",
+                }
+            except Exception as e:                      # context only: never costs the bench line
+                res["cpu_baseline"]["all_cores"] = {"error": str(e)[-300:]}
     return res
 
 
@@ -833,6 +919,8 @@ def main():
                          "and print its report; a small case for profiling the prefill kernel")
     ap.add_argument("--cpu-seqs", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-all-cores-budget", type=float, default=6.0,
+                    help="seconds of timed passes of the oracle on all host cores (0: skip)")
     ap.add_argument("--ref-seqs", type=int, default=32)
     ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core", "tensor_core_head_batched"],
                     help="kernel family of paged_attention_decode (auto: tensor cores)")

@@ -37,3 +37,17 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_all_cores_oracle_pass_uses_every_core_and_cleans_up():
+    # The bench's second CPU figure: the oracle over the same sample on a
+    # spawn pool with one single-threaded process per host core.
+    import glob
+    import tempfile
+    sys.path.insert(0, ROOT)
+    import bench
+    before = set(glob.glob(os.path.join(tempfile.gettempdir(), "pk_oracle_pool_*")))
+    r = bench.run_cpu_oracle_pool("tiny", 0, 4, 0.3)
+    assert r["cores"] == len(os.sched_getaffinity(0))
+    assert r["seqs"] == 4 and r["bytes"] > 0 and len(r["times"]) >= 1 and min(r["times"]) > 0
+    assert set(glob.glob(os.path.join(tempfile.gettempdir(), "pk_oracle_pool_*"))) == before
