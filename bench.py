@@ -405,10 +405,22 @@ def workload_report(name, seed, dev, steps, flush, peak):
                                      w.scale, w.block_size, w.max_seq_len, ws)
     for _ in range(3):
         fn()
-    ms = time_decode(fn, steps, flush, torch.cuda.current_stream(dev))
+    stream = torch.cuda.current_stream(dev)
+    ms = time_decode(fn, steps, flush, stream)
     gbs = ub["attention"] / (ms * 1e-3) / 1e9
     rep = {"decode_ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
            "tokens_per_s_per_layer": round(w.num_seqs / (ms * 1e-3), 1)}
+    # The cache writes alone (each call repeats the same copies and writes, so
+    # it is idempotent); GB/s of bytes read plus written.
+    if w.copy_pairs.shape[0]:
+        cms = time_decode(lambda: pk.copy_blocks(t["k_cache"], t["v_cache"], t["copy_pairs"]), steps, flush, stream)
+        rep["copy_blocks_us"] = round(cms * 1e3, 2)
+        rep["copy_blocks_gbs"] = round(ub["copies"] / (cms * 1e-3) / 1e9, 1)
+    if w.num_new_tokens:
+        ams = time_decode(lambda: pk.reshape_and_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"],
+                                                       t["slot_mapping"]), steps, flush, stream)
+        rep["reshape_and_cache_us"] = round(ams * 1e3, 2)
+        rep["reshape_and_cache_gbs"] = round(ub["append"] / (ams * 1e-3) / 1e9, 1)
     if ub["kv_unique"] != ub["kv"]:
         uniq = (ub["attention"] - ub["kv"] + ub["kv_unique"]) / (ms * 1e-3) / 1e9
         rep["gbs_unique_bytes"] = round(uniq, 1)
@@ -816,6 +828,16 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    pre_bytes = ub["append"] + ub["copies"]
+    pre_ms = statistics.median([e[0].elapsed_time(e[1]) for e in ev])
+    if pre_bytes > 0 and pre_ms > 0:
+        res["cache_ops"] = {
+            "what": "copy_blocks (the copy-on-write pairs, if any) then reshape_and_cache of each timed step, "
+                    "between the same events (L2 cold before each step); bytes read plus written",
+            "us_per_step": round(pre_ms * 1e3, 2),
+            "bytes_per_step": pre_bytes,
+            "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
+        }
     if others:
         res["other_workloads"] = others
     if multi:
