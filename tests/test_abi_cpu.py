@@ -160,6 +160,45 @@ def test_multi_query_host_validation(lib):
         assert call() == -7
 
 
+
+def test_swap_blocks_host_validation(lib):
+    f = lib.pk_swap_blocks
+
+    def call(dk="fake", n=2, hkv=8, d=128, b=16, src_nb=32, dst_nb=16, dst_k_off=0):
+        dk = ctypes.c_void_p(_fake().value + dst_k_off) if dk == "fake" else dk
+        return f(dk, _fake(), _fake(), _fake(), _fake(), n, hkv, d, b, src_nb, dst_nb, None)
+    assert call(n=-1) == -2
+    assert call(src_nb=-1) == -2 and call(dst_nb=-1) == -2
+    assert call(hkv=0) == -2 and call(b=0) == -2
+    assert call(d=96) == -3                                   # head_dim
+    assert call(b=12) == -3                                   # block size
+    assert call(n=0) == 0                                     # no pairs: a no-op
+    assert call(dk=NULL) == -1
+    assert call(dst_k_off=8) == -6                            # not 16-byte aligned
+    if not torch.cuda.is_available():
+        assert call() == -7                                   # valid, but no device here
+
+
+def test_decode_noalloc_host_validation(lib):
+    f = lib.pk_paged_attention_decode_noalloc
+
+    def call(out="fake", dt=0, n=2, h=8, hkv=2, d=128, b=16, mb=4, msl=64, scale=0.088, q_off=0):
+        out = _fake() if out == "fake" else out
+        return f(out, dt, ctypes.c_void_p(_fake().value + q_off), _fake(), _fake(), _fake(), mb, _fake(), msl,
+                 n, h, hkv, d, 16, b, scale, None)
+    assert call(h=6, hkv=4) == -2                             # heads not a multiple of kv heads
+    assert call(msl=65) == -2                                 # longer than the table can hold
+    assert call(n=-1) == -2 and call(n=65536) == -2
+    assert call(scale=float("inf")) == -2
+    assert call(dt=7) == -3 and call(d=96) == -3 and call(b=64) == -3
+    assert call(h=24, hkv=8) == -3                            # group of 3
+    assert call(n=0) == 0                                     # empty batch: a no-op
+    assert call(out=NULL) == -1
+    assert call(q_off=2) == -6                                # not 16-byte aligned
+    if not torch.cuda.is_available():
+        assert call() == -7                                   # valid, but no device here
+
+
 def test_binding_refuses_cpu_tensors():
     import paged_kv_cache_122_gb300 as pk
     q = torch.zeros(1, 8, 64, dtype=torch.bfloat16)
