@@ -646,9 +646,7 @@ def run_ours(args):
     max_tiles = w.num_seqs * w.num_kv_heads * ((w.max_seq_len + 127) // 128)
     tensor_core = args.decode_path.startswith("tensor_core") or \
         (args.decode_path == "auto" and max_tiles >= torch.cuda.get_device_properties(dev).multi_processor_count)
-    head_batched = args.decode_path == "tensor_core_head_batched" and w.num_kv_heads == 8 and \
-        w.block_size in (16, 32) and w.group <= 8
-    merge = (not head_batched) and w.max_seq_len > (128 if tensor_core else 512)   # fused when head-batched
+    merge = w.max_seq_len > (128 if tensor_core else 512)
     launches_per_step = (1 if w.copy_pairs.shape[0] else 0) + (1 if w.num_new_tokens else 0) + 1 + (1 if merge else 0)
 
     for _ in range(args.warmup):
@@ -944,7 +942,7 @@ def main():
     ap.add_argument("--cpu-all-cores-budget", type=float, default=6.0,
                     help="seconds of timed passes of the oracle on all host cores (0: skip)")
     ap.add_argument("--ref-seqs", type=int, default=32)
-    ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core", "tensor_core_head_batched"],
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core"],
                     help="kernel family of paged_attention_decode (auto: tensor cores)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps

@@ -224,13 +224,8 @@ enum pk_decode_path {
                                             group size, CUDA cores for a batch too
                                             small to give each SM one 128-token tile */
     PK_PATH_CUDA_CORE = 1,               /* fp32 FMA on CUDA cores, one CTA per partition */
-    PK_PATH_TENSOR_CORE = 2,             /* tcgen05 MMA, persistent CTAs, tiles of
+    PK_PATH_TENSOR_CORE = 2              /* tcgen05 MMA, persistent CTAs, tiles of
                                             128 tokens x 1 KV head */
-    PK_PATH_TENSOR_CORE_HEAD_BATCHED = 3 /* tcgen05 MMA, persistent CTAs, tiles of
-                                            16 tokens x all KV heads, merge fused into the
-                                            kernel; used where it applies (num_kv_heads == 8,
-                                            block_size 16 or 32, G <= 8), per-head tiles
-                                            otherwise */
 };
 
 /*

@@ -81,7 +81,7 @@ STATUS_NAMES = {
 PK_ERR_NO_BLOCKS, PK_ERR_UNKNOWN_SEQUENCE, PK_ERR_SEQUENCE_EXISTS = -8, -9, -10
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 DEVERR_POINTER = 0x20
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_TENSOR_CORE_HEAD_BATCHED = 0, 1, 2, 3
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
 
 _lib = None
 

@@ -329,14 +329,13 @@ def pk_gather_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: tor
 
 
 def pk_set_decode_path(path) -> int:
-    """Choose the decode kernel: "auto", "cuda_core", "tensor_core" or
-    "tensor_core_head_batched" (or 0/1/2/3).
+    """Choose the decode kernel: "auto", "cuda_core" or "tensor_core" (or
+    0/1/2).
 
     Returns the previous setting as an int.
     """
     names = {"auto": _native.PATH_AUTO, "cuda_core": _native.PATH_CUDA_CORE,
-             "tensor_core": _native.PATH_TENSOR_CORE,
-             "tensor_core_head_batched": _native.PATH_TENSOR_CORE_HEAD_BATCHED}
+             "tensor_core": _native.PATH_TENSOR_CORE}
     code = names[path] if isinstance(path, str) else int(path)
     prev = load().pk_set_decode_path(code)
     if prev < 0:

@@ -27,11 +27,8 @@ struct DecodeParams {
     float *ws_o;
     int part_tokens;   // tokens per partition (multiple of 128)
     int np_cap;        // partitions reserved per (sequence, head)
-    // Tensor-core paths: two cut-segment slots per CTA (head-batched: then
-    // one ticket per CTA).
+    // Tensor-core path: two cut-segment slots per CTA.
     void *tc_slots;
-    // Head-batched path: tag of this call for the merge tickets (never 0).
-    uint32_t epoch;
     // Multi-query attention (tensor-core path): q is [total_q, H, D] and
     // sequence s owns query rows cu_q_lens[s] .. cu_q_lens[s+1]-1, its newest
     // tokens, causal among themselves; q_len is the padded number of query
@@ -65,12 +62,6 @@ size_t tc_slot_bytes();
 // Tensor-core path with an explicit grid of `ctas` persistent CTAs; the
 // slots at p.tc_slots must hold 2 * ctas slots.
 cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas);
-
-// Tensor-core path with head-batched tiles (8 KV heads, block size 16 or 32,
-// G <= 8): one segment per sequence, merge fused into the kernel.
-bool hb_supported(int num_heads, int num_kv_heads, int head_dim, int block_size);
-size_t hb_workspace_bytes();
-cudaError_t launch_decode_head_batched(const DecodeParams &p, cudaStream_t stream);
 
 // CUDA-core path (any supported G).  Returns a cudaError_t.
 cudaError_t launch_decode_cuda_core(const DecodeParams &p, cudaStream_t stream);

@@ -36,14 +36,11 @@ extern "C" size_t pk_decode_workspace_bytes(int num_seqs, int num_heads, int num
     // Enough for either kernel family (the family can be switched at run time).
     const size_t cc = np_cap > 1 ? pk::workspace_floats(num_seqs, num_heads, head_dim, np_cap) * sizeof(float) : 0;
     const size_t tc = max_seq_len > 128 ? pk::tc_workspace_bytes() : 0;
-    const size_t hb = max_seq_len > 16 && pk::hb_supported(num_heads, num_kv_heads, head_dim, 16)
-                          ? pk::hb_workspace_bytes() : 0;
-    return std::max(cc, std::max(tc, hb));
+    return std::max(cc, tc);
 }
 
 extern "C" int pk_set_decode_path(int path) {
-    if (path != PK_PATH_AUTO && path != PK_PATH_CUDA_CORE && path != PK_PATH_TENSOR_CORE &&
-        path != PK_PATH_TENSOR_CORE_HEAD_BATCHED)
+    if (path != PK_PATH_AUTO && path != PK_PATH_CUDA_CORE && path != PK_PATH_TENSOR_CORE)
         return PK_ERR_UNSUPPORTED;
     return g_path.exchange(path);
 }
@@ -100,15 +97,11 @@ extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q
     const int64_t max_tiles = static_cast<int64_t>(num_seqs) * num_kv_heads * ceil_div(max_seq_len, 128);
     const bool tiny = max_tiles < pk::sm_count();
     const bool tensor_core = max_seq_len > 0 &&
-        (path == PK_PATH_TENSOR_CORE || path == PK_PATH_TENSOR_CORE_HEAD_BATCHED ||
-         (path == PK_PATH_AUTO && G >= kTensorCoreMinGroup && !tiny));
-    const bool head_batched = path == PK_PATH_TENSOR_CORE_HEAD_BATCHED && tensor_core &&
-                              pk::hb_supported(num_heads, num_kv_heads, head_dim, block_size);
+        (path == PK_PATH_TENSOR_CORE || (path == PK_PATH_AUTO && G >= kTensorCoreMinGroup && !tiny));
     if (tensor_core) {
         // A sequence longer than one tile may span several CTAs: its parts need slots.
-        const int tile = head_batched ? 16 : 128;
-        const size_t need = head_batched ? pk::hb_workspace_bytes() : pk::tc_workspace_bytes();
-        if (max_seq_len > tile) {
+        const size_t need = pk::tc_workspace_bytes();
+        if (max_seq_len > 128) {
             if (!workspace || workspace_bytes < need) return PK_ERR_WORKSPACE;
             if (!pk::aligned16(workspace)) return PK_ERR_ALIGNMENT;
             p.tc_slots = workspace;
@@ -131,7 +124,6 @@ extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q
     p.err = pk::error_word_ptr();
     if (!p.err) return PK_ERR_NO_DEVICE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (head_batched) return pk::launch_decode_head_batched(p, st) == cudaSuccess ? PK_OK : PK_ERR_CUDA;
     if (tensor_core) return pk::launch_decode_tensor_core(p, st) == cudaSuccess ? PK_OK : PK_ERR_CUDA;
     if (pk::launch_decode_cuda_core(p, st) != cudaSuccess) return PK_ERR_CUDA;
     if (pk::launch_decode_merge(p, st) != cudaSuccess) return PK_ERR_CUDA;

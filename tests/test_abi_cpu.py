@@ -53,18 +53,18 @@ def test_status_strings_and_version(lib):
         assert lib.pk_status_string(code)
     assert lib.pk_status_string(12345) == b"unknown status"
     assert lib.pk_set_decode_path(7) == -3
+    assert lib.pk_set_decode_path(3) == -3            # the removed head-batched family
     assert lib.pk_set_decode_path(1) == 0 and lib.pk_set_decode_path(0) == 1
 
 
 def test_workspace_bound(lib):
     f = lib.pk_decode_workspace_bytes
     slots = 2 * 1024 * 8384                             # per-head tensor-core kernel: 2 slots per CTA
-    hb = 2 * 1024 * 33344 + 1024 * 8                    # head-batched kernel: 2 slots + 1 ticket per CTA
     assert f(4, 8, 8, 64, 16) == 0                      # every sequence fits one tile: nothing is split
     assert f(4, 8, 2, 64, 128) == 0
     assert f(4, 8, 2, 64, 129) == slots                 # 2 KV heads: per-head tiles of 128 tokens
-    assert f(4, 8, 8, 64, 17) == hb                     # 8 KV heads: head-batched tiles of 16 tokens
-    assert f(8, 32, 8, 128, 131072) == max(8 * 32 * 512 * 130 * 4, slots, hb)
+    assert f(4, 8, 8, 64, 129) == slots                 # 8 KV heads: the same
+    assert f(8, 32, 8, 128, 131072) == max(8 * 32 * 512 * 130 * 4, slots)
     assert f(1, 6, 4, 128, 4096) == 0                   # 6 % 4 != 0
     assert f(1, 8, 8, 96, 4096) == 0                    # head_dim unsupported
     assert f(-1, 8, 8, 64, 10) == 0

@@ -13,7 +13,7 @@ from paritylib import assert_close, host_bits
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-PATHS = ["cuda_core", "tensor_core", "tensor_core_head_batched"]
+PATHS = ["cuda_core", "tensor_core"]
 
 
 @pytest.fixture
