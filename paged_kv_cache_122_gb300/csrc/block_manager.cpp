@@ -66,6 +66,18 @@ struct Undo {
     int32_t old_block; // kind 2: the shared block that was replaced
 };
 
+// Room for one more entry in a table, allocated before a block is taken so
+// that nothing can throw between taking a block and recording it.
+bool reserve_one(std::vector<int32_t> &v) {
+    if (v.size() < v.capacity()) return true;
+    try {
+        v.reserve(v.empty() ? 8 : 2 * v.capacity());
+        return true;
+    } catch (...) {
+        return false;
+    }
+}
+
 template <typename F>
 int guarded(F &&f) {
     try {
@@ -130,6 +142,10 @@ extern "C" int pk_bm_append_slots(pk_block_manager *bm, const int64_t *seq_ids, 
             if (off == 0) {                                    // the token starts a new block
                 if (bm->count == 0) {
                     status = PK_ERR_NO_BLOCKS;
+                    break;
+                }
+                if (!reserve_one(sq.table)) {                  // undone below like any failure
+                    status = PK_ERR_HOST_MEMORY;
                     break;
                 }
                 sq.table.push_back(bm->take());

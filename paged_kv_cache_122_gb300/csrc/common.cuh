@@ -69,4 +69,8 @@ unsigned int *error_word_ptr();
 // Multiprocessor count of the current device (0 on failure).
 int sm_count();
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Raise the dynamic shared memory limit of `func` to `bytes` on the current
+// device.  The attribute is per device, so it is set once for every (device,
+// kernel) pair; thread-safe.
+cudaError_t set_max_dynamic_smem(const void *func, int bytes);
 }  // namespace pk

@@ -73,7 +73,7 @@ extern "C" int pk_paged_attention_decode_noalloc(void *out, int out_dtype, const
     if (block_size != 8 && block_size != 16 && block_size != 32) return PK_ERR_UNSUPPORTED;
     if (!group_ok(num_heads / num_kv_heads)) return PK_ERR_UNSUPPORTED;
     if (!std::isfinite(scale)) return PK_ERR_SHAPE;
-    if (num_seqs > 65535) return PK_ERR_SHAPE;
+    if (num_seqs > 65535 || num_kv_heads * 2 > 65535) return PK_ERR_SHAPE;
     if (num_seqs == 0) return PK_OK;
     if (!out || !q || !seq_lens || (max_seq_len > 0 && (!k_cache || !v_cache || !block_tables)))
         return PK_ERR_NULL;

@@ -928,15 +928,11 @@ bool encode_q_map(CUtensorMap *m, const DecodeParams &p) {
 template <int D, int NC>
 cudaError_t launch_dg(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const DecodeParams &p,
                       int C, cudaStream_t stream) {
-    static bool attr_set = false;   // per instantiation; setting it twice is harmless
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, NC, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_tc_kernel<D, NC, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kSmemBytes));
+    {
+        cudaError_t e = p.cu_q_lens
+            ? set_max_dynamic_smem(reinterpret_cast<const void *>(decode_tc_kernel<D, NC, true>), static_cast<int>(kSmemBytes))
+            : set_max_dynamic_smem(reinterpret_cast<const void *>(decode_tc_kernel<D, NC, false>), static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -2,6 +2,8 @@
 #include "common.cuh"
 
 #include <mutex>
+#include <set>
+#include <utility>
 
 namespace {
 
@@ -13,6 +15,7 @@ constexpr int kMaxDevices = 64;
 unsigned int *g_error_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 std::mutex g_mu;
+std::set<std::pair<int, const void *>> g_smem_attr_done;   // (device, kernel) pairs already raised
 
 int current_device() {
     int dev = -1;
@@ -52,6 +55,20 @@ int sm_count() {
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];
+}
+
+cudaError_t set_max_dynamic_smem(const void *func, int bytes) {
+    const int dev = current_device();
+    if (dev < 0) {
+        cudaGetLastError();
+        return cudaErrorNoDevice;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_smem_attr_done.count({dev, func})) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    g_smem_attr_done.insert({dev, func});
+    return cudaSuccess;
 }
 
 }  // namespace pk

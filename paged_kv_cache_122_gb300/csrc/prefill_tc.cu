@@ -690,12 +690,10 @@ cudaError_t launch_dg(const DecodeParams &p, int max_q_len, cudaStream_t stream)
     int o_tma = 0;
     if (!p.out_fp32 && encode(&mo, p.out, 3, qdims, qstr, qbox)) o_tma = 1;
     else mo = mq;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+    {
+        const cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(prefill_tc_kernel<D, G>),
+                                                   static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     const int qblocks = (max_q_len + 2 * (kRows / G) - 1) / (2 * (kRows / G));
     const int64_t grid = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * qblocks;

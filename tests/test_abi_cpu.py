@@ -189,6 +189,7 @@ def test_decode_noalloc_host_validation(lib):
     assert call(h=6, hkv=4) == -2                             # heads not a multiple of kv heads
     assert call(msl=65) == -2                                 # longer than the table can hold
     assert call(n=-1) == -2 and call(n=65536) == -2
+    assert call(h=40000, hkv=40000) == -2                     # the regular call's KV-head bound
     assert call(scale=float("inf")) == -2
     assert call(dt=7) == -3 and call(d=96) == -3 and call(b=64) == -3
     assert call(h=24, hkv=8) == -3                            # group of 3

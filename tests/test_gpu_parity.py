@@ -1,11 +1,11 @@
 """GPU parity: every workload's decode step through the C ABI against the
 float64 oracle on the same seeded inputs.
 
-Small workloads are compared element by element over every sequence.  The
-Llama-3-70B-shaped batch and the long-context batch run at full size in the
-launch configuration the bench times; the oracle then checks a sample of
-sequences (always including the shortest and the longest), and the cache
-writes are checked bit for bit over the whole pool.
+Every workload, the Llama-3-70B-shaped batch and the long-context batch
+included, runs at full size in the launch configuration the bench times, and
+its output is compared with the oracle element by element over every
+sequence; seeds 1 and 2 repeat that on every workload.  The cache writes are
+checked bit for bit over the whole pool.
 """
 import numpy as np
 import pytest
@@ -20,16 +20,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def _run(name, seed, out_dtype, sample=None):
+def _run(name, seed, out_dtype):
     w = W.get(name, seed)
     t = W.make_tensors(w, DEV)
     pre = pre_step_host(t)
     out = gpu_step(w, t, out_dtype)
     torch.cuda.synchronize()
-    ref, kc, vc = oracle_step(w, pre, seqs=sample)
-    rows = list(range(w.num_seqs)) if sample is None else list(sample)
-    g = out.float().cpu().numpy()[rows]
-    err = assert_close(g, ref[rows], out_dtype == torch.bfloat16, f"{name} seed {seed}")
+    ref, kc, vc = oracle_step(w, pre)
+    g = out.float().cpu().numpy()
+    err = assert_close(g, ref, out_dtype == torch.bfloat16, f"{name} seed {seed}")
     # The caches after the step equal the oracle's, bit for bit, over the whole pool.
     assert np.array_equal(host_bits(t["k_cache"]), kc)
     assert np.array_equal(host_bits(t["v_cache"]), vc)
@@ -38,35 +37,19 @@ def _run(name, seed, out_dtype, sample=None):
     return err
 
 
+ALL = ["tiny", "l3-8b", "l3-70b", "long", "prefix-b8", "prefix-b16", "prefix-b32"]
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("name", ["tiny", "l3-8b", "prefix-b8", "prefix-b16", "prefix-b32"])
+@pytest.mark.parametrize("name", ALL)
 def test_full_parity(name, out_dtype):
     _run(name, 0, out_dtype)
 
 
 @pytest.mark.parametrize("seed", [1, 2])
-def test_full_parity_more_seeds(seed):
-    _run("tiny", seed, torch.float32)
-    _run("prefix-b16", seed, torch.bfloat16)
-
-
-def _sample(w, k, seed):
-    rng = np.random.default_rng(seed)
-    L = w.seq_lens
-    picks = {int(np.argmin(L)), int(np.argmax(L))}
-    picks.update(int(x) for x in rng.choice(w.num_seqs, size=min(k, w.num_seqs), replace=False))
-    return sorted(picks)
-
-
-@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_llama3_70b_full_size_sampled(out_dtype):
-    w = W.get("l3-70b", 0)
-    _run("l3-70b", 0, out_dtype, sample=_sample(w, 24, 7))
-
-
-def test_long_context_full_size_sampled():
-    w = W.get("long", 0)
-    _run("long", 0, torch.float32, sample=_sample(w, 1, 8))
+@pytest.mark.parametrize("name", ALL)
+def test_full_parity_more_seeds(name, seed):
+    _run(name, seed, torch.bfloat16 if seed == 1 else torch.float32)
 
 
 @pytest.mark.parametrize("name", ["tiny", "prefix-b8", "prefix-b32"])
