@@ -392,8 +392,8 @@ def workload_report(name, seed, dev, steps, flush, peak):
     w = W.get(name, seed)
     t = W.make_tensors(w, dev)
     ub = M.useful_bytes(w)
-    ws = torch.empty(max(1, pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
-                                                        w.max_seq_len)), dtype=torch.uint8, device=dev)
+    ws = pk.new_workspace((pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                        w.max_seq_len)), dev)
     out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
     if w.copy_pairs.shape[0]:
         pk.copy_blocks(t["k_cache"], t["v_cache"], t["copy_pairs"])
@@ -622,11 +622,16 @@ def run_ours(args):
     pk.load_library()
     pk.pk_set_decode_path(args.decode_path)
     w = W.get(args.workload, args.seed + rank)
+    if args.shape:
+        # The workload's lengths with other head counts / head dim (kernel
+        # comparisons): attention only, no appends or copies.
+        H, Hkv, D = (int(x) for x in args.shape.split(":"))
+        w = W.custom(args.seed + rank, w.seq_lens, H, Hkv, D, w.block_size)
     t = W.make_tensors(w, dev)
     ub = M.useful_bytes(w)
     out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
     ws_bytes = pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.max_seq_len)
-    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    workspace = pk.new_workspace(ws_bytes, dev)
     stream = torch.cuda.current_stream(dev)
     flush = L2Flush(dev)
 
@@ -765,7 +770,8 @@ def run_ours(args):
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     attn_gbs = ub["attention"] / (attn_avg_ms * 1e-3) / 1e9
     traffic = None
-    if RECORDED_TRAFFIC["sources_sha1"] == sources_sha1() and RECORDED_TRAFFIC["workload"] == args.workload:
+    if (RECORDED_TRAFFIC["sources_sha1"] == sources_sha1() and RECORDED_TRAFFIC["workload"] == args.workload
+            and not args.shape):
         traffic = RECORDED_TRAFFIC["bytes_per_launch"]
     res = {
         "metric": METRIC,
@@ -781,7 +787,9 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}",
+            "workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}" + (
+                f"; its lengths with {w.num_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
+                "attention only" if args.shape else ""),
             "num_seqs": w.num_seqs, "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": w.block_size, "num_blocks": w.num_blocks,
             "tokens_attended": ub["tokens"], "new_tokens": w.num_new_tokens,
@@ -890,10 +898,12 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    # Each step: the oracle over a bounded sample of the workload (first
-    # --ref-seqs sequences); warm-up passes are discarded.
-    r = run_cpu_oracle(args.workload, args.seed, args.ref_seqs, budget_s=1e9,
-                       max_reps=args.steps + args.warmup)
+    # Each step: the oracle over a bounded sample of the workload (its first
+    # --ref-seqs sequences; by default as many as keep the whole run near a
+    # minute: 32 at 20 steps, one at 640 steps or more); warm-up passes are
+    # discarded.
+    nseq = args.ref_seqs if args.ref_seqs > 0 else max(1, min(32, 640 // (args.steps + args.warmup)))
+    r = run_cpu_oracle(args.workload, args.seed, nseq, budget_s=1e9, max_reps=args.steps + args.warmup)
     times = r["times"][args.warmup:] or r["times"]
     tot = sum(times)
     value = r["bytes"] * len(times) / tot / 1e9
@@ -923,7 +933,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="l3-70b", choices=sorted(WORKLOAD_DESC))
     ap.add_argument("--seed", type=int, default=0)
@@ -937,11 +947,15 @@ def main():
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill workload (16 x 512-token chunks over 4096 earlier tokens) "
                          "and print its report; a small case for profiling the prefill kernel")
+    ap.add_argument("--shape", default="",
+                    help="H:Hkv:D -- the workload's sequence lengths with these head counts and head dim "
+                         "(attention only; for kernel comparisons such as small groups or head dim 64)")
     ap.add_argument("--cpu-seqs", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--cpu-all-cores-budget", type=float, default=6.0,
                     help="seconds of timed passes of the oracle on all host cores (0: skip)")
-    ap.add_argument("--ref-seqs", type=int, default=32)
+    ap.add_argument("--ref-seqs", type=int, default=0,
+                    help="sequences per step of the reference arm (0: sized from --steps, see run_reference)")
     ap.add_argument("--decode-path", default="auto", choices=["auto", "cuda_core", "tensor_core"],
                     help="kernel family of paged_attention_decode (auto: tensor cores)")
     args = ap.parse_args()

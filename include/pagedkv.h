@@ -91,14 +91,20 @@ const char *pk_status_string(int status);
 int pk_version(void);
 
 /*
- * Bytes of workspace pk_paged_attention_decode needs for these sizes.
+ * Bytes of workspace pk_paged_attention_decode (and
+ * pk_paged_attention_multi_query) needs for these sizes; 0 when no sequence
+ * can be split (max_seq_len <= 128) or the sizes are invalid.
  *
- * The workspace holds the split-K partial results of long sequences: for every
- * (sequence, KV head, partition) the running max and denominator of each of the
- * G query heads and their unnormalised output rows, all fp32.  It is sized for
- * the worst case the host can see (every sequence as long as max_seq_len), so
- * the call never needs to read seq_lens on the host.  Returns 0 for invalid
- * sizes.
+ * The workspace holds split-K partial results.  On the tensor-core kernel
+ * (the default) a sequence longer than one 128-token tile may be cut across
+ * CTAs of the persistent grid; each CTA has two 8,384-byte slots for the
+ * parts it cuts (a header; per column the max and denominator; the
+ * unnormalised output rows), so it needs 2 x 1,024 x 8,384 = 17,170,432
+ * bytes whatever the sizes.  The CUDA-core kernel keeps (max, denominator,
+ * output row) per (sequence, query head, 512-token partition) instead.  The
+ * workspace is sized for the larger of the two, and for the worst case the
+ * host can see (every sequence as long as max_seq_len), so the call never
+ * reads seq_lens on the host.
  */
 size_t pk_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
                                  int head_dim, int max_seq_len);
@@ -186,6 +192,35 @@ int pk_paged_attention_decode_noalloc(void *out, int out_dtype, const void *q,
                                       float scale, pk_stream_t stream);
 
 /*
+ * Self-test of the kernels' bounded waits; the pages have no counterpart.
+ *
+ * Every wait of the tensor-core decode kernel on one of its own pipeline
+ * barriers gives up after a time limit (1 s in normal calls), sets
+ * PK_DEVERR_TIMEOUT, lets the CTA's own copies and MMAs land, frees its tensor
+ * memory and returns, so a pipeline that stops never hangs the GPU.  This
+ * call runs pk_paged_attention_decode on the tensor-core kernel with the
+ * limit set to wait_limit_us and with CTA 0's copy producer stopping before
+ * tile `stall_tile` of its range, so that CTA's waits on that tile's barriers
+ * run out and take the give-up path.  Afterwards pk_get_device_error reports
+ * PK_DEVERR_TIMEOUT and the output is invalid; the next call on the same
+ * context and workspace is correct.
+ *
+ *   stall_tile     >= 1 (a tile of CTA 0's range; beyond its range nothing stalls)
+ *   wait_limit_us  in [100, 1000000]
+ *   everything else as for pk_paged_attention_decode.
+ * Returns PK_ERR_SHAPE for a bad stall_tile or wait_limit_us.
+ */
+int pk_selftest_decode_wait_timeout(void *out, int out_dtype, const void *q,
+                                    const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int max_blocks_per_seq,
+                                    const int32_t *seq_lens, int max_seq_len,
+                                    int num_seqs, int num_heads, int num_kv_heads,
+                                    int head_dim, int num_blocks, int block_size,
+                                    float scale, void *workspace, size_t workspace_bytes,
+                                    int stall_tile, unsigned int wait_limit_us,
+                                    pk_stream_t stream);
+
+/*
  * Attention of SEVERAL new tokens per sequence over the paged cache, causal
  * among them: chunked prefill of a prompt ("PagedAttention from First
  * Principles", §12) and speculative-decoding verification, where the
@@ -232,8 +267,9 @@ enum pk_decode_path {
  * Select the decode kernel family for later calls (all devices); returns the
  * previous setting, or PK_ERR_UNSUPPORTED for an unknown value.  Both
  * families compute the same attention; they differ in how the score and
- * output contractions are executed.  Not synchronised with calls in flight on
- * other host threads.
+ * output contractions are executed.  The setting is process-wide: do not
+ * change it while another host thread may be issuing decode calls (each call
+ * reads it once, so a call racing with the change may use either family).
  */
 int pk_set_decode_path(int path);
 

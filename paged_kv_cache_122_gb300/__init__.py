@@ -15,6 +15,7 @@ the first call does, and fails loudly if it has not been built.
 from .api import (  # noqa: F401
     LayerPointers,
     copy_blocks,
+    new_workspace,
     paged_attention_decode,
     paged_attention_multi_query,
     pk_paged_attention_multi_query,
@@ -26,6 +27,7 @@ from .api import (  # noqa: F401
     pk_paged_attention_decode,
     pk_reshape_and_cache,
     pk_reshape_and_cache_layers,
+    pk_selftest_decode_wait_timeout,
     pk_set_decode_path,
     pk_swap_blocks,
     reshape_and_cache,

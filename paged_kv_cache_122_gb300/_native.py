@@ -28,6 +28,10 @@ SIGNATURES = {
     "pk_paged_attention_decode_noalloc": (c_int, [
         c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
         c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p]),
+    "pk_selftest_decode_wait_timeout": (c_int, [
+        c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
+        c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+        c_void_p, c_size_t, c_int, c_uint, c_void_p]),   # workspace, bytes, stall_tile, wait_limit_us, stream
     "pk_paged_attention_multi_query": (c_int, [
         c_void_p, c_int, c_void_p, c_int,      # out, out_dtype, q, total_q
         c_void_p, c_int,                       # cu_q_lens, max_q_len

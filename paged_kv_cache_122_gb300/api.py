@@ -47,6 +47,12 @@ def pk_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int, 
     return int(load().pk_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len))
 
 
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A decode workspace of ``nbytes`` (at least one byte; its contents on
+    entry do not matter to the C call)."""
+    return torch.empty(max(1, nbytes), dtype=torch.uint8, device=device)
+
+
 def workspace_for(device: torch.device, nbytes: int, stream=None) -> Optional[torch.Tensor]:
     """A cached scratch buffer of at least ``nbytes`` for ``device`` and stream."""
     if nbytes == 0:
@@ -55,7 +61,7 @@ def workspace_for(device: torch.device, nbytes: int, stream=None) -> Optional[to
     key = (device, s.cuda_stream)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        ws = new_workspace(nbytes, device)
         _WORKSPACES[key] = ws
     return ws
 
@@ -100,6 +106,25 @@ def pk_paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch
             _stream(dev, stream))
     check("pk_paged_attention_decode", st)
     return out
+
+
+def pk_selftest_decode_wait_timeout(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                    v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                    scale: float, max_seq_len: int, workspace: torch.Tensor, stall_tile: int,
+                                    wait_limit_us: int, stream=None) -> int:
+    """Self-test of the bounded waits (see the C header): a decode call on the
+    tensor-core kernel whose CTA 0 stops issuing copies at ``stall_tile``, so
+    its waits give up after ``wait_limit_us``.  Returns the call's status."""
+    dev = q.device
+    N, H, D = q.shape
+    P, B, Hkv, _ = k_cache.shape
+    with torch.cuda.device(dev):
+        return int(load().pk_selftest_decode_wait_timeout(
+            _ptr(out), _native.PK_FP32 if out.dtype == torch.float32 else _native.PK_BF16, _ptr(q),
+            _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+            int(max_seq_len), N, H, Hkv, D, P, B, float(scale), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), int(stall_tile), int(wait_limit_us),
+            _stream(dev, stream)))
 
 
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -29,6 +29,11 @@ struct DecodeParams {
     int np_cap;        // partitions reserved per (sequence, head)
     // Tensor-core path: two cut-segment slots per CTA.
     void *tc_slots;
+    // Bounded waits: give up after this many ns (0 = the default, 1 s).
+    uint64_t wait_limit_ns;
+    // Self-test of the bounded waits: when > 0, CTA 0's producer issues no
+    // copy from this tile of its range on, so its consumers' waits run out.
+    int stall_tile;
     // Multi-query attention (tensor-core path): q is [total_q, H, D] and
     // sequence s owns query rows cu_q_lens[s] .. cu_q_lens[s+1]-1, its newest
     // tokens, causal among themselves; q_len is the padded number of query
@@ -55,6 +60,8 @@ cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t s
 // Multi-query attention for wide query blocks (chunked prefill): 128 query
 // rows (128 / G tokens x G heads) per CTA over the paged keys; no workspace.
 cudaError_t launch_prefill_tensor_core(const DecodeParams &p, int max_q_len, cudaStream_t stream);
+// Largest persistent grid of the tensor-core path.
+constexpr int kTcMaxCtas = 1024;
 // Workspace bytes the tensor-core path needs (independent of the sizes).
 size_t tc_workspace_bytes();
 // Bytes of one cut-segment slot of the tensor-core path (two per CTA).

@@ -70,10 +70,7 @@ constexpr uint32_t kQOff = 4 * kChunkBytes;
 constexpr uint32_t kQChunkBytes = kNPad * 128;
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + 2 * kQChunkBytes;
 constexpr uint32_t kPBytes = kTile * kNPad * 2;
-constexpr uint32_t kTmemCols = 64;                           // S^T x2 (16 cols), O^T x2 (16 cols)
-constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 32;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s: far beyond any legal wait
+constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s: far beyond any legal wait (default)
 
 constexpr uint32_t kIdescQK = idesc_bf16(kTile, kNPad, 0, 0);   // A = K (K-major), B = Q (K-major)
 constexpr uint32_t kIdescPV = idesc_bf16(128, kNPad, 1, 1);     // A = V^T (MN-major), B = P^T (MN-major)
@@ -105,29 +102,30 @@ struct Misc {
 
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 2 * kPBytes + sizeof(Misc);
 
-// Workspace slot of a cut segment.
+// Workspace slot of a cut segment's part: slot 0 of a CTA holds the part of
+// its first segment, slot 1 the part of its last one.
 struct Slot {
-    int32_t flag;          // slot 0 only: 1 = this CTA merges the segment
+    int32_t flag;          // slot 0 only: 1 = the merge kernel's CTA c combines this segment
     int32_t s, h;
     int32_t first_cta;     // slot 0 only: the CTA in whose range the segment starts
     int64_t start_tile;    // flattened index of the segment's (s, h) tile 0
     int64_t total_tiles;
     int64_t range_beg;     // slot 0 only: first tile of this CTA's range
     int64_t pad2[3];
-    float m[kNPad];
-    float l[kNPad];
-    float o[kNPad * 128];
+    float m[kNPad];        // reference max per column (base 2)
+    float l[kNPad];        // denominator per column
+    float o[kNPad * 128];  // unnormalised output, [column][O^T row]
 };
-constexpr size_t kMaxCtas = 1024;
+constexpr size_t kMaxCtas = kTcMaxCtas;
 
 __device__ __forceinline__ int clamp_len(const DecodeParams &p, int s, int cap) {
     const int raw = p.seq_lens[s];
     return raw < 0 ? 0 : (raw > cap ? cap : raw);
 }
 
-// Walks the flattened (sequence, KV head, tile) space in order.
+// Walks the flattened (sequence, KV head group, tile) space in order.
 struct Walk {
-    int s, h, t, nt, L;
+    int s, h, t, nt, L, nh;          // nh: KV head groups per sequence
     __device__ __forceinline__ void load(const DecodeParams &p, int cap) {
         L = clamp_len(p, s, cap);
         nt = (L + kTile - 1) / kTile;
@@ -135,7 +133,7 @@ struct Walk {
     __device__ __forceinline__ void next(const DecodeParams &p, int cap) {
         if (++t < nt) return;
         t = 0;
-        if (++h < p.num_kv_heads) return;
+        if (++h < nh) return;
         h = 0;
         do {
             if (++s >= p.num_seqs) return;
@@ -173,13 +171,27 @@ __device__ __forceinline__ void store_out(const DecodeParams &p, size_t idx, flo
     else static_cast<uint16_t *>(p.out)[idx] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
 }
 
-template <int D, int NC, bool MQ>
+// HP KV heads per tile: HP = 2 pairs two adjacent KV heads at head dim 64,
+// so that each token's page row is one 256-byte piece (the two heads side by
+// side in the cache) instead of two 128-byte pieces 1 KiB apart.
+template <int D, int NC, bool MQ, int HP>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(NC >= 1 && NC <= kNPad, "group");
-    constexpr int NCH = D / 64;
+    static_assert(HP == 1 || (HP == 2 && D == 64 && NC <= 8), "head pairs: head dim 64, at most 8 columns each");
+    constexpr int NCH = D * HP / 64;                  // 128-byte chunks of a tile row
+    // TMEM: S^T double-buffered (16 columns per head of the tile), then O^T
+    // double-buffered by segment (16 columns).  P and O columns: HP == 1,
+    // column g = query column g; HP == 2, columns 0-7 belong to the pair's
+    // first head and 8-15 to its second, NC query columns each (the rest
+    // padding); O^T rows are then (head of the pair, head-dim element).
+    constexpr uint32_t kSCols = 16 * HP;
+    constexpr uint32_t tS = 0, tO = 2 * kSCols;
+    constexpr uint32_t kTmemCols = HP == 2 ? 128 : 64;
+    constexpr int CW = HP == 2 ? 8 : kNPad;           // P columns per head of the tile
+    constexpr int NCOL = HP == 2 ? 8 + NC : NC;       // columns 0 .. NCOL-1 may be in use
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -191,9 +203,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x, C = gridDim.x;
-    const int N = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads, B = p.block_size;
+    // Hkv counts the tile's KV head groups (segments per sequence).
+    const int N = p.num_seqs, Hkv = p.num_kv_heads / HP, H = p.num_heads, B = p.block_size;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * B);
-    const int Gq = H / Hkv, lgG = __ffs(Gq) - 1;     // query heads per KV head (a power of two)
+    const int Gq = H / p.num_kv_heads, lgG = __ffs(Gq) - 1;     // query heads per KV head (a power of two)
     // K and V of a tile in shared memory: each page in one TMA box as B / 8
     // blocks of 8 rows, each block [half][8 rows][64] -- so the 8-row
     // swizzle atoms of one 64-element half lie kAtomStride bytes apart
@@ -201,6 +214,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     constexpr uint32_t kAtomStride = 1024u * NCH;
     constexpr bool mq = MQ;                           // several query tokens per sequence
     Slot *slots = static_cast<Slot *>(p.tc_slots);
+    const uint64_t lim = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -335,6 +349,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const uint32_t tmem = misc->tmem_base;
 
     Walk w0{};
+    w0.nh = Hkv;
     if (n_tiles > 0) {
         w0.s = misc->s0;
         w0.load(p, cap);
@@ -356,7 +371,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         };
         int phys_next = n_tiles > 0 ? fetch(w) : -1;
         int seg_i0 = 0;
+        bool stalled = false;
         for (int i = 0; i < n_tiles; ++i) {
+            // Self-test of the bounded waits: CTA 0 stops issuing here, so
+            // the barriers of this tile never complete.
+            if (p.stall_tile > 0 && c == 0 && i == p.stall_tile) {
+                stalled = true;
+                break;
+            }
             if (i == 0 || w.t == 0) seg_i0 = i;
             // The stage still holds this segment's queries from tile i - kStages.
             const bool q_resident = i - seg_i0 >= kStages;
@@ -364,7 +386,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const int phys_raw = phys_next;
             int got = 1;
             if (lane == 0)
-                got = mbar_wait(smem_u32(&misc->empty[st]), ((i / kStages) & 1) ^ 1, &misc->abort, kWaitLimitNs);
+                got = mbar_wait(smem_u32(&misc->empty[st]), ((i / kStages) & 1) ^ 1, &misc->abort, lim);
             if (!__shfl_sync(0xffffffffu, got, 0)) {      // one decision for the whole warp
                 if (lane == 0) {
                     misc->abort = 1;
@@ -419,10 +441,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (lane == 0 && !q_resident) {
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
+                    // Chunk ch: elements 64 ch .. 64 ch + 63 of the KV head's
+                    // queries (HP == 1), or all 64 of the pair's head ch (HP == 2).
+                    const int qx = HP == 2 ? 0 : ch * 64;
+                    const int qh = (w.h * HP + (HP == 2 ? ch : 0)) * Gq;
                     if constexpr (MQ)   // box (64, G heads, q_len tokens): column r * G + g
-                        tma_load_3d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, ch * 64, w.h * Gq, qrow0);
+                        tma_load_3d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, qx, qh, qrow0);
                     else      // box (64, 16 rows) of the [N * H, D] queries
-                        tma_load_2d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, ch * 64, w.s * H + w.h * Gq);
+                        tma_load_2d(sbase + kQOff + ch * kQChunkBytes, &tm_q, full, qx, w.s * H + qh);
                 }
             }
             if (ok) {
@@ -435,11 +461,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             w.next(p, cap);
             if (i + 1 < n_tiles) phys_next = fetch(w);
         }
-        // On abort, let this warp's copies land before the CTA can exit.
-        if (misc->abort && lane == 0) {
+        // On abort (or a self-test stall), let this warp's copies land before
+        // the CTA can exit.
+        if ((misc->abort || stalled) && lane == 0) {
             for (int i = max(0, issued - kStages); i < issued; ++i) {
-                mbar_wait(smem_u32(&misc->full[i % kStages]), (i / kStages) & 1, &misc->never, kWaitLimitNs);
-                mbar_wait(smem_u32(&misc->vfull[i % kStages]), (i / kStages) & 1, &misc->never, kWaitLimitNs);
+                mbar_wait(smem_u32(&misc->full[i % kStages]), (i / kStages) & 1, &misc->never, lim);
+                mbar_wait(smem_u32(&misc->vfull[i % kStages]), (i / kStages) & 1, &misc->never, lim);
             }
         }
     } else if (warp == 1) {
@@ -459,7 +486,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     // two 64-element halves 1,024 bytes apart.
                     const uint64_t a = smem_desc(vbase + kk * 2 * kAtomStride, 1024, kAtomStride, kLayoutSw128);
                     const uint64_t b = smem_desc(pbase + kk * 512, 256, 128, kLayoutNone);
-                    mma_bf16(tmem + kTmemO + (sg & 1) * kNPad, a, b, kIdescPV, (first && kk == 0) ? 0u : 1u);
+                    mma_bf16(tmem + tO + (sg & 1) * kNPad, a, b, kIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(smem_u32(&misc->o_full[pb]));
                 mma_commit(smem_u32(&misc->empty[j % kStages]));
@@ -473,14 +500,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const uint32_t sbase = stage_addr + st * kStageBytes;
                 const int sb = i & 1;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    // K: the half (kk / 4) of each 8-row block, 1,024 bytes in
-                    // for the second; atoms kAtomStride apart.
+                for (int kk = 0; kk < NCH * 4; ++kk) {
+                    // K: the chunk (kk / 4) of each 8-row block, 1,024 bytes in
+                    // for the second; atoms kAtomStride apart.  HP == 2: chunk
+                    // kk / 4 is head kk / 4 of the pair, whose scores go to
+                    // their own 16 columns.
                     const uint32_t off = (kk >> 2) * 1024u + (kk & 3) * 32;
                     const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
                     const uint64_t a = smem_desc(sbase + kKOff + off, 16, kAtomStride, kLayoutSw128);
                     const uint64_t b = smem_desc(sbase + kQOff + qoff, 16, 1024, kLayoutSw128);
-                    mma_bf16(tmem + kTmemS + sb * kNPad, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+                    const uint32_t dcol = tS + sb * kSCols + (HP == 2 ? (kk >> 2) * 16u : 0u);
+                    const bool acc = HP == 2 ? (kk & 3) > 0 : kk > 0;
+                    mma_bf16(tmem + dcol, a, b, kIdescQK, acc ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&misc->s_full[sb]));
             };
@@ -512,7 +543,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 } else if ((++spins & 255u) == 0) {
                     const uint64_t now = globaltimer_ns();
                     if (spins == 256) t_idle = now;
-                    else if (misc->abort || now - t_idle > kWaitLimitNs) {
+                    else if (misc->abort || now - t_idle > lim) {
                         misc->abort = 1;
                         set_error(p.err, PK_DEVERR_TIMEOUT);
                         break;
@@ -521,7 +552,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             }
             // Let every issued MMA finish before the CTA can release TMEM.
             mma_commit(smem_u32(&misc->drain));
-            mbar_wait(smem_u32(&misc->drain), 0, &misc->never, kWaitLimitNs);
+            mbar_wait(smem_u32(&misc->drain), 0, &misc->never, lim);
         }
         __syncwarp();
     } else {
@@ -535,9 +566,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        float m_ref[NC], l_run[NC], m_prev[NC], l_prev[NC];
+        float m_ref[NCOL], l_run[NCOL], m_prev[NCOL], l_prev[NCOL];
 #pragma unroll
-        for (int g = 0; g < NC; ++g) m_ref[g] = l_run[g] = m_prev[g] = l_prev[g] = 0.f;
+        for (int j = 0; j < NCOL; ++j) m_ref[j] = l_run[j] = m_prev[j] = l_prev[j] = 0.f;
+        // This thread's TMEM lane as an O^T row: the head-dim element (HP ==
+        // 1), or (head of the pair, element) = (row / 64, row % 64) (HP == 2).
+        const int hr = HP == 2 ? row >> 6 : 0;
+        const int dd = HP == 2 ? (row & 63) : row;
+        const bool row_ok = HP == 2 || row < D;
+        // Query column c of this row's head, from a 16-column row of O or l.
+        auto colv = [&](const float (&v)[kNPad], int cq) -> float {
+            if constexpr (HP == 2) return hr ? v[CW + cq] : v[cq];
+            else return v[cq];
+        };
         int seg = -1, seg_t0 = 0, seg_i0 = 0;
         bool pending = false;            // a finished segment awaits its read-out
         int pend_seg = 0, pend_s = 0, pend_h = 0, pend_i = 0, pend_t0 = 0, pend_i0 = 0, pend_q0 = 0, pend_qn = 1;
@@ -545,52 +586,51 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         auto finalize = [&]() -> bool {
             // P.V of the segment's last tile (pend_i) complete.
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[pend_i & 1]), (pend_i >> 1) & 1,
-                                                   &misc->never, kWaitLimitNs)))
+                                                   &misc->never, lim)))
                 return false;
             tc_fence_after();
-            float ov[16];
-            tmem_ld16(lane_addr + kTmemO + (pend_seg & 1) * kNPad, ov);
+            float ov[kNPad];
+            tmem_ld16(lane_addr + tO + (pend_seg & 1) * kNPad, ov);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&misc->o_free[pend_seg & 1]));
 #pragma unroll
-            for (int g = 0; g < NC; ++g) {
-                const float v = warp_sum(l_prev[g]);
-                if (lane == 0) misc->lsum[quad][g] = v;
+            for (int j = 0; j < NCOL; ++j) {
+                const float v = warp_sum(l_prev[j]);
+                if (lane == 0) misc->lsum[quad][j] = v;
             }
             named_bar_sync(1, 128);
-            float l[NC];
+            float l[kNPad];
 #pragma unroll
-            for (int g = 0; g < NC; ++g)
-                l[g] = misc->lsum[0][g] + misc->lsum[1][g] + misc->lsum[2][g] + misc->lsum[3][g];
+            for (int j = 0; j < kNPad; ++j)
+                l[j] = j < NCOL ? misc->lsum[0][j] + misc->lsum[1][j] + misc->lsum[2][j] + misc->lsum[3][j] : 0.f;
             if (pend_complete) {
-                if (row < D) {
+                if (row_ok) {
 #pragma unroll
-                    for (int g = 0; g < NC; ++g) {
-                        if constexpr (MQ) {
-                            // Column g: query token g / G (padded columns past the
-                            // sequence's queries are not written), head g % G.
-                            if ((g >> lgG) >= pend_qn) continue;
-                            store_out(p, (static_cast<size_t>(pend_q0 + (g >> lgG)) * H + pend_h * Gq + (g & (Gq - 1))) * D + row,
-                                      l[g] > 0.f ? ov[g] / l[g] : 0.f);
-                        } else {
-                            store_out(p, (static_cast<size_t>(pend_s) * H + pend_h * NC + g) * D + row,
-                                      l[g] > 0.f ? ov[g] / l[g] : 0.f);
-                        }
+                    for (int cq = 0; cq < NC; ++cq) {
+                        // Column cq: query token cq / G (multi-query; padded
+                        // columns past the sequence's queries are not
+                        // written), query head cq % G of this row's KV head.
+                        if ((cq >> lgG) >= pend_qn) continue;
+                        const float lv = colv(l, cq);
+                        const size_t qrow = static_cast<size_t>(MQ ? pend_q0 : pend_s) + (cq >> lgG);
+                        const int qh = (pend_h * HP + hr) * Gq + (cq & (Gq - 1));
+                        store_out(p, (qrow * H + qh) * D + dd, lv > 0.f ? colv(ov, cq) / lv : 0.f);
                     }
                 }
             } else {
+                // A cut part: slot 0 if the segment is this CTA's first, 1 if not.
                 const int slot_idx = pend_i0 == 0 ? 0 : 1;
                 Slot *sl = slots + 2 * c + slot_idx;
-                if (row < D) {
+                if (row_ok) {
 #pragma unroll
-                    for (int g = 0; g < NC; ++g) sl->o[g * D + row] = ov[g];
+                    for (int cq = 0; cq < NC; ++cq) sl->o[(hr * CW + cq) * 128 + row] = colv(ov, cq);
                 }
                 if (row == 0) {
 #pragma unroll
-                    for (int g = 0; g < NC; ++g) {
-                        sl->m[g] = m_prev[g];
-                        sl->l[g] = l[g];
+                    for (int j = 0; j < NCOL; ++j) {
+                        sl->m[j] = m_prev[j];
+                        sl->l[j] = l[j];
                     }
                     sl->s = pend_s;
                     sl->h = pend_h;
@@ -610,7 +650,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const int st = i % kStages;
             const int sb = i & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->s_full[sb]), (i >> 1) & 1, &misc->never,
-                                                   kWaitLimitNs))) {
+                                                   lim))) {
                 misc->abort = 1;
                 set_error(p.err, PK_DEVERR_TIMEOUT);
                 break;
@@ -625,63 +665,80 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 seg_t0 = mt.z;
                 seg_i0 = i;
 #pragma unroll
-                for (int g = 0; g < NC; ++g) {
-                    m_ref[g] = -INFINITY;
-                    l_run[g] = 0.f;
+                for (int j = 0; j < NCOL; ++j) {
+                    m_ref[j] = -INFINITY;
+                    l_run[j] = 0.f;
                 }
             }
             tc_fence_after();
-            float sv[16];
-            tmem_ld16(lane_addr + kTmemS + sb * kNPad, sv);
+            float sv[kNPad];
+            if constexpr (HP == 2) {
+                // The pair's scores: columns 0-7 of each head's 16.
+                float s0[8], s1[8];
+                tmem_ld<8>(lane_addr + tS + sb * kSCols, s0);
+                tmem_ld<8>(lane_addr + tS + sb * kSCols + 16, s1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    sv[j] = s0[j];
+                    sv[8 + j] = s1[j];
+                }
+            } else {
+                tmem_ld16(lane_addr + tS + sb * kSCols, sv);
+            }
             const bool valid = (misc->mask[st][row >> 5] >> (row & 31)) & 1u;
-            float s2[NC];
+            float s2[NCOL];
             bool need = false;
             const int jpos = mt.z * kTile + row;          // this row's token position
 #pragma unroll
-            for (int g = 0; g < NC; ++g) {
-                // Multi-query: column g is query token g / G, which sees positions <= its own.
-                const bool vg = valid && (!mq || jpos <= qm.z + (g >> lgG));
-                s2[g] = vg ? sv[g] * p.scale_log2 : -INFINITY;
-                need |= s2[g] > m_ref[g] + kRescaleLog2;
+            for (int j = 0; j < NCOL; ++j) {
+                if ((j % CW) >= NC) {                      // padding column of a head pair
+                    s2[j] = -INFINITY;
+                    continue;
+                }
+                // Multi-query: query column j % CW is query token (j % CW) / G,
+                // which sees positions <= its own.
+                const bool vg = valid && (!mq || jpos <= qm.z + ((j % CW) >> lgG));
+                s2[j] = vg ? sv[j] * p.scale_log2 : -INFINITY;
+                need |= s2[j] > m_ref[j] + kRescaleLog2;
             }
             if (named_bar_or(1, 128, need)) {
                 // Rare: move the reference to the running max.
 #pragma unroll
-                for (int g = 0; g < NC; ++g) {
-                    const float mx = warp_max_redux(s2[g]);
-                    if (lane == 0) misc->red[quad][g] = mx;
+                for (int j = 0; j < NCOL; ++j) {
+                    const float mx = warp_max_redux(s2[j]);
+                    if (lane == 0) misc->red[quad][j] = mx;
                 }
                 named_bar_sync(1, 128);
-                float a[NC];
+                float a[NCOL];
 #pragma unroll
-                for (int g = 0; g < NC; ++g) {
-                    const float t = fmaxf(fmaxf(misc->red[0][g], misc->red[1][g]),
-                                          fmaxf(misc->red[2][g], misc->red[3][g]));
-                    const float mn = fmaxf(m_ref[g], t);
-                    a[g] = m_ref[g] == -INFINITY ? 0.f : fast_exp2(m_ref[g] - mn);
-                    l_run[g] *= a[g];
-                    m_ref[g] = mn;
+                for (int j = 0; j < NCOL; ++j) {
+                    const float t = fmaxf(fmaxf(misc->red[0][j], misc->red[1][j]),
+                                          fmaxf(misc->red[2][j], misc->red[3][j]));
+                    const float mn = fmaxf(m_ref[j], t);
+                    a[j] = m_ref[j] == -INFINITY ? 0.f : fast_exp2(m_ref[j] - mn);
+                    l_run[j] *= a[j];
+                    m_ref[j] = mn;
                 }
                 if (!seg_first) {
                     // O through tile i-1, in TMEM (thread <-> head-dim row).
                     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[(i - 1) & 1]), ((i - 1) >> 1) & 1,
-                                                           &misc->never, kWaitLimitNs))) {
+                                                           &misc->never, lim))) {
                         misc->abort = 1;
                         set_error(p.err, PK_DEVERR_TIMEOUT);
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t oaddr = lane_addr + kTmemO + (seg & 1) * kNPad;
+                    const uint32_t oaddr = lane_addr + tO + (seg & 1) * kNPad;
                     float ov[16];
                     tmem_ld16(oaddr, ov);
                     float lo[8], hi[8];
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        lo[g] = g < NC ? ov[g] * a[g < NC ? g : 0] : ov[g];
-                        hi[g] = 8 + g < NC ? ov[8 + g] * a[8 + g < NC ? 8 + g : 0] : ov[8 + g];
+                    for (int j = 0; j < 8; ++j) {
+                        lo[j] = j < NCOL ? ov[j] * a[j < NCOL ? j : 0] : ov[j];
+                        hi[j] = 8 + j < NCOL ? ov[8 + j] * a[8 + j < NCOL ? 8 + j : 0] : ov[8 + j];
                     }
                     tmem_st8(oaddr, lo);
-                    if (NC > 8) tmem_st8(oaddr + 8, hi);
+                    if (NCOL > 8) tmem_st8(oaddr + 8, hi);
                 }
                 // red[] is rewritten only in a later rare path, after the next vote.
             }
@@ -689,20 +746,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
             for (int g = 0; g < kNPad; ++g) pr[g] = 0.f;
 #pragma unroll
-            for (int g = 0; g < NC; ++g) {
-                if constexpr (MQ) pr[g] = s2[g] != -INFINITY ? fast_exp2(s2[g] - m_ref[g]) : 0.f;
-                else pr[g] = valid ? fast_exp2(s2[g] - m_ref[g]) : 0.f;
+            for (int j = 0; j < NCOL; ++j) {
+                if ((j % CW) >= NC) continue;              // padding column: weight 0
+                if constexpr (MQ) pr[j] = s2[j] != -INFINITY ? fast_exp2(s2[j] - m_ref[j]) : 0.f;
+                else pr[j] = valid ? fast_exp2(s2[j] - m_ref[j]) : 0.f;
             }
             uint32_t packed[kNPad / 2];
 #pragma unroll
             for (int gp = 0; gp < kNPad / 2; ++gp) packed[gp] = pack_bf16x2(pr[2 * gp], pr[2 * gp + 1]);
             // The denominator sums the bf16 weights the MMA actually applies.
 #pragma unroll
-            for (int g = 0; g < NC; ++g)
-                l_run[g] += (g & 1) ? bf16_hi(packed[g >> 1]) : bf16_lo(packed[g >> 1]);
+            for (int j = 0; j < NCOL; ++j)
+                l_run[j] += (j & 1) ? bf16_hi(packed[j >> 1]) : bf16_lo(packed[j >> 1]);
             // P buffer sb is free once P.V of tile i-2 is done.
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->o_full[sb]), ((i >> 1) & 1) ^ 1, &misc->never,
-                                                   kWaitLimitNs))) {
+                                                   lim))) {
                 misc->abort = 1;
                 set_error(p.err, PK_DEVERR_TIMEOUT);
                 break;
@@ -710,7 +768,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             // Rows of masked tokens are zeroed once this tile's V has landed.
             if (__any_sync(0xffffffffu, !valid) &&
                 !__all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->vfull[st]), (i / kStages) & 1, &misc->never,
-                                                   kWaitLimitNs))) {
+                                                   lim))) {
                 misc->abort = 1;
                 set_error(p.err, PK_DEVERR_TIMEOUT);
                 break;
@@ -753,9 +811,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 pend_complete = seg_t0 == 0 && mt.z == mt.w - 1;
                 pend_cut_end = mt.z == mt.w - 1;
 #pragma unroll
-                for (int g = 0; g < NC; ++g) {
-                    m_prev[g] = m_ref[g];
-                    l_prev[g] = l_run[g];
+                for (int j = 0; j < NCOL; ++j) {
+                    m_prev[j] = m_ref[j];
+                    l_prev[j] = l_run[j];
                 }
                 if (i == n_tiles - 1 && !finalize()) {
                     misc->abort = 1;
@@ -774,17 +832,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
 }
 
-// One CTA per main-kernel CTA c: if c's first segment was cut at its start
-// and ends in c, combine the parts of that segment from every CTA it spans.
-template <int D, int NC>
+// One CTA per decode CTA c: if c's first segment was cut at its start and
+// ends in c, combine the parts of that segment from every CTA it spans.
+// Thread r handles O^T row r (as the decode kernel's TMEM lanes).
+template <int D, int NC, int HP>
 __global__ void __launch_bounds__(128)
 decode_tc_merge_kernel(const DecodeParams p, int C) {
+    constexpr int CW = HP == 2 ? 8 : kNPad;
     // Launched as a programmatic dependent of the decode grid: wait for it
     // to finish and its writes to be visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const Slot *slots = static_cast<const Slot *>(p.tc_slots);
     const int c = blockIdx.x;
-    const int d = threadIdx.x < D ? threadIdx.x : D - 1;
+    const int row = threadIdx.x;
+    const int hr = HP == 2 ? row >> 6 : 0;           // head of the pair (HP == 2)
+    const int dd = HP == 2 ? (row & 63) : row;       // head-dim element
+    const bool row_ok = HP == 2 || row < D;
+    const int orow = row_ok ? row : 0;
     const Slot *mine = slots + 2 * c;
     // Everything the common case needs (this CTA's slot 0 and both slots of
     // CTA c - 1) is loaded at once, before the flag is known.
@@ -797,18 +861,19 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
     const int64_t beg_prev = q0->range_beg;
     float mm[NC], ml[NC], mo[NC], am[NC], al[NC], ao[NC], bm[NC], bl[NC], bo[NC];
 #pragma unroll
-    for (int g = 0; g < NC; ++g) {
-        mm[g] = mine->m[g];
-        ml[g] = mine->l[g];
-        mo[g] = mine->o[g * D + d];
-        am[g] = q0->m[g];
-        al[g] = q0->l[g];
-        ao[g] = q0->o[g * D + d];
-        bm[g] = q1->m[g];
-        bl[g] = q1->l[g];
-        bo[g] = q1->o[g * D + d];
+    for (int cq = 0; cq < NC; ++cq) {
+        const int j = hr * CW + cq;
+        mm[cq] = mine->m[j];
+        ml[cq] = mine->l[j];
+        mo[cq] = mine->o[j * 128 + orow];
+        am[cq] = q0->m[j];
+        al[cq] = q0->l[j];
+        ao[cq] = q0->o[j * 128 + orow];
+        bm[cq] = q1->m[j];
+        bl[cq] = q1->l[j];
+        bo[cq] = q1->o[j * 128 + orow];
     }
-    if (flag != 1 || threadIdx.x >= D) return;
+    if (flag != 1 || !row_ok) return;
     // First tile of CTA cc's range (the decode grid wrote it into slot 0).
     auto range_beg = [&](int cc) -> int64_t { return cc < C ? slots[2 * cc].range_beg : T; };
     float num[NC], den[NC];
@@ -816,14 +881,14 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
         // Two parts: CTA c - 1 (slot 0 if the segment is its first, else 1) and this CTA.
         const bool first_of_prev = beg_prev >= start;
 #pragma unroll
-        for (int g = 0; g < NC; ++g) {
-            const float pm = first_of_prev ? am[g] : bm[g];
-            const float pl = first_of_prev ? al[g] : bl[g];
-            const float po = first_of_prev ? ao[g] : bo[g];
-            const float M = fmaxf(pm, mm[g]);
-            const float a0 = rescale(pm, M), a1 = rescale(mm[g], M);
-            den[g] = a0 * pl + a1 * ml[g];
-            num[g] = a0 * po + a1 * mo[g];
+        for (int cq = 0; cq < NC; ++cq) {
+            const float pm = first_of_prev ? am[cq] : bm[cq];
+            const float pl = first_of_prev ? al[cq] : bl[cq];
+            const float po = first_of_prev ? ao[cq] : bo[cq];
+            const float M = fmaxf(pm, mm[cq]);
+            const float a0 = rescale(pm, M), a1 = rescale(mm[cq], M);
+            den[cq] = a0 * pl + a1 * ml[cq];
+            num[cq] = a0 * po + a1 * mo[cq];
         }
     } else {
         // Contributors are the CTAs from ca to c with a non-empty range (when
@@ -831,35 +896,38 @@ decode_tc_merge_kernel(const DecodeParams p, int C) {
         // no slot).
         float M[NC];
 #pragma unroll
-        for (int g = 0; g < NC; ++g) M[g] = -INFINITY;
+        for (int cq = 0; cq < NC; ++cq) M[cq] = -INFINITY;
         for (int cc = ca; cc <= c; ++cc) {
             if (range_beg(cc) == range_beg(cc + 1)) continue;
             const Slot *sl = slots + 2 * cc + (range_beg(cc) >= start ? 0 : 1);
 #pragma unroll
-            for (int g = 0; g < NC; ++g) M[g] = fmaxf(M[g], sl->m[g]);
+            for (int cq = 0; cq < NC; ++cq) M[cq] = fmaxf(M[cq], sl->m[hr * CW + cq]);
         }
 #pragma unroll
-        for (int g = 0; g < NC; ++g) num[g] = den[g] = 0.f;
+        for (int cq = 0; cq < NC; ++cq) num[cq] = den[cq] = 0.f;
         for (int cc = ca; cc <= c; ++cc) {
             if (range_beg(cc) == range_beg(cc + 1)) continue;
             const Slot *sl = slots + 2 * cc + (range_beg(cc) >= start ? 0 : 1);
 #pragma unroll
-            for (int g = 0; g < NC; ++g) {
-                const float a = rescale(sl->m[g], M[g]);
-                den[g] = fmaf(a, sl->l[g], den[g]);
-                num[g] = fmaf(a, sl->o[g * D + d], num[g]);
+            for (int cq = 0; cq < NC; ++cq) {
+                const int j = hr * CW + cq;
+                const float a = rescale(sl->m[j], M[cq]);
+                den[cq] = fmaf(a, sl->l[j], den[cq]);
+                num[cq] = fmaf(a, sl->o[j * 128 + row], num[cq]);
             }
         }
     }
-    // Column g: query token g / G of the sequence, head g % G (as in the decode kernel).
+    // Column cq: query token cq / G of the sequence, query head cq % G of
+    // this row's KV head (as in the decode kernel).
     const int Gq = p.num_heads / p.num_kv_heads, lgG = __ffs(Gq) - 1;
     const int q0row = p.cu_q_lens ? p.cu_q_lens[s] : s;
     const int qn = p.cu_q_lens ? p.cu_q_lens[s + 1] - q0row : 1;
 #pragma unroll
-    for (int g = 0; g < NC; ++g) {
-        if ((g >> lgG) >= qn) continue;
-        store_out(p, (static_cast<size_t>(q0row + (g >> lgG)) * p.num_heads + h * Gq + (g & (Gq - 1))) * D + d,
-                  den[g] > 0.f ? num[g] / den[g] : 0.f);
+    for (int cq = 0; cq < NC; ++cq) {
+        if ((cq >> lgG) >= qn) continue;
+        const int qh = (h * HP + hr) * Gq + (cq & (Gq - 1));
+        store_out(p, (static_cast<size_t>(q0row + (cq >> lgG)) * p.num_heads + qh) * D + dd,
+                  den[cq] > 0.f ? num[cq] / den[cq] : 0.f);
     }
 }
 
@@ -880,18 +948,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-// K or V pages: one box per (page, KV head) holding its B rows as B / 8
-// blocks of 8 rows, each block [half][8 rows][64] in shared memory
-// (dimensions: 64 elements; row within the block; 64-element half, 128
-// bytes apart; 8-row block, numbered page * B / 8 + block; KV head).
-bool encode_page_map(CUtensorMap *m, const void *base, const DecodeParams &p) {
+// K or V pages: one box per (page, group of HP adjacent KV heads) holding
+// its B rows as B / 8 blocks of 8 rows, each block [chunk][8 rows][64] in
+// shared memory (dimensions: 64 elements; row within the block; 128-byte
+// chunk of the group's row -- a 64-element half of the head, or (HP = 2,
+// head dim 64) one head of the pair; 8-row block, numbered page * B / 8 +
+// block; KV head group).
+bool encode_page_map(CUtensorMap *m, const void *base, const DecodeParams &p, int hp) {
     auto enc = get_encoder();
     if (!enc) return false;
-    const cuuint64_t D = p.head_dim, Hkv = p.num_kv_heads, B = p.block_size;
+    const cuuint64_t D = p.head_dim, Hkv = p.num_kv_heads, B = p.block_size, HP = hp;
     const cuuint64_t P = p.num_blocks > 0 ? p.num_blocks : 1;
-    cuuint64_t dims[5] = {64, 8, D / 64, P * (B / 8), Hkv};
-    cuuint64_t strides[4] = {Hkv * D * 2, 128, 8 * Hkv * D * 2, D * 2};
-    cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(D / 64), static_cast<cuuint32_t>(B / 8), 1};
+    cuuint64_t dims[5] = {64, 8, D * HP / 64, P * (B / 8), Hkv / HP};
+    cuuint64_t strides[4] = {Hkv * D * 2, 128, 8 * Hkv * D * 2, HP * D * 2};
+    cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(D * HP / 64), static_cast<cuuint32_t>(B / 8), 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -925,13 +995,17 @@ bool encode_q_map(CUtensorMap *m, const DecodeParams &p) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int NC>
-cudaError_t launch_dg(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const DecodeParams &p,
-                      int C, cudaStream_t stream) {
+template <int D, int NC, int HP>
+cudaError_t launch_dg(const DecodeParams &p, int C, cudaStream_t stream) {
+    CUtensorMap mk, mv, mq;
+    if (!encode_page_map(&mk, p.k_cache, p, HP) || !encode_page_map(&mv, p.v_cache, p, HP) || !encode_q_map(&mq, p))
+        return cudaErrorInvalidValue;
     {
-        cudaError_t e = p.cu_q_lens
-            ? set_max_dynamic_smem(reinterpret_cast<const void *>(decode_tc_kernel<D, NC, true>), static_cast<int>(kSmemBytes))
-            : set_max_dynamic_smem(reinterpret_cast<const void *>(decode_tc_kernel<D, NC, false>), static_cast<int>(kSmemBytes));
+        const cudaError_t e = p.cu_q_lens
+            ? set_max_dynamic_smem(reinterpret_cast<const void *>(decode_tc_kernel<D, NC, true, HP>),
+                                   static_cast<int>(kSmemBytes))
+            : set_max_dynamic_smem(reinterpret_cast<const void *>(decode_tc_kernel<D, NC, false, HP>),
+                                   static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
     }
     cudaLaunchAttribute attr[1];
@@ -944,25 +1018,44 @@ cudaError_t launch_dg(const CUtensorMap &mk, const CUtensorMap &mv, const CUtens
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = p.cu_q_lens ? cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NC, true>, mk, mv, mq, p)
-                                : cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NC, false>, mk, mv, mq, p);
+    const cudaError_t e = p.cu_q_lens ? cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NC, true, HP>, mk, mv, mq, p)
+                                      : cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NC, false, HP>, mk, mv, mq, p);
     if (e != cudaSuccess) return e;
     if (!p.tc_slots) return cudaSuccess;   // no sequence longer than one tile: nothing is cut
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, decode_tc_merge_kernel<D, NC>, p, C);
+    return cudaLaunchKernelEx(&cfg, decode_tc_merge_kernel<D, NC, HP>, p, C);
 }
 
-template <int D>
-cudaError_t launch_d(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const DecodeParams &p,
-                     int C, cudaStream_t stream) {
+// Head dim 64 with at most 8 columns per KV head and an even number of KV
+// heads: tiles of two adjacent KV heads (256-byte page rows).
+template <int NC>
+cudaError_t launch_d64(const DecodeParams &p, int C, cudaStream_t stream) {
+    if constexpr (NC <= 8) {
+        if (p.num_kv_heads % 2 == 0) return launch_dg<64, NC, 2>(p, C, stream);
+    }
+    return launch_dg<64, NC, 1>(p, C, stream);
+}
+
+cudaError_t launch_any(const DecodeParams &p, int C, cudaStream_t stream) {
     // MMA columns: the group's query heads times the query tokens per sequence.
-    switch ((p.num_heads / p.num_kv_heads) * (p.cu_q_lens ? p.q_len : 1)) {
-        case 1: return launch_dg<D, 1>(mk, mv, mq, p, C, stream);
-        case 2: return launch_dg<D, 2>(mk, mv, mq, p, C, stream);
-        case 4: return launch_dg<D, 4>(mk, mv, mq, p, C, stream);
-        case 8: return launch_dg<D, 8>(mk, mv, mq, p, C, stream);
-        case 16: return launch_dg<D, 16>(mk, mv, mq, p, C, stream);
+    const int nc = (p.num_heads / p.num_kv_heads) * (p.cu_q_lens ? p.q_len : 1);
+    if (p.head_dim == 64) {
+        switch (nc) {
+            case 1: return launch_d64<1>(p, C, stream);
+            case 2: return launch_d64<2>(p, C, stream);
+            case 4: return launch_d64<4>(p, C, stream);
+            case 8: return launch_d64<8>(p, C, stream);
+            case 16: return launch_d64<16>(p, C, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (nc) {
+        case 1: return launch_dg<128, 1, 1>(p, C, stream);
+        case 2: return launch_dg<128, 2, 1>(p, C, stream);
+        case 4: return launch_dg<128, 4, 1>(p, C, stream);
+        case 8: return launch_dg<128, 8, 1>(p, C, stream);
+        case 16: return launch_dg<128, 16, 1>(p, C, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -972,13 +1065,10 @@ cudaError_t launch_d(const CUtensorMap &mk, const CUtensorMap &mv, const CUtenso
 size_t tc_workspace_bytes() { return 2 * kMaxCtas * sizeof(Slot); }
 
 cudaError_t launch_decode_tensor_core(const DecodeParams &p, cudaStream_t stream) {
-    CUtensorMap mk, mv, mq;
-    if (!encode_page_map(&mk, p.k_cache, p) || !encode_page_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
-        return cudaErrorInvalidValue;
     int C = sm_count();
     if (C <= 0) return cudaErrorNoDevice;
     if (C > static_cast<int>(kMaxCtas)) C = static_cast<int>(kMaxCtas);
-    return p.head_dim == 64 ? launch_d<64>(mk, mv, mq, p, C, stream) : launch_d<128>(mk, mv, mq, p, C, stream);
+    return launch_any(p, C, stream);
 }
 
 }  // namespace pk
@@ -995,11 +1085,8 @@ cudaError_t launch_multi_query_tensor_core(const DecodeParams &p, cudaStream_t s
 }
 
 cudaError_t launch_decode_tensor_core_grid(const DecodeParams &p, cudaStream_t stream, int ctas) {
-    CUtensorMap mk, mv, mq;
     if (ctas <= 0 || ctas > static_cast<int>(kMaxCtas)) return cudaErrorInvalidValue;
-    if (!encode_page_map(&mk, p.k_cache, p) || !encode_page_map(&mv, p.v_cache, p) || !encode_q_map(&mq, p))
-        return cudaErrorInvalidValue;
-    return p.head_dim == 64 ? launch_d<64>(mk, mv, mq, p, ctas, stream) : launch_d<128>(mk, mv, mq, p, ctas, stream);
+    return launch_any(p, ctas, stream);
 }
 
 }  // namespace pk

@@ -59,11 +59,11 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_bound(lib):
     f = lib.pk_decode_workspace_bytes
-    slots = 2 * 1024 * 8384                             # per-head tensor-core kernel: 2 slots per CTA
+    slots = 2 * 1024 * 8384                             # tensor-core kernel: 2 slots per CTA
     assert f(4, 8, 8, 64, 16) == 0                      # every sequence fits one tile: nothing is split
     assert f(4, 8, 2, 64, 128) == 0
     assert f(4, 8, 2, 64, 129) == slots                 # 2 KV heads: per-head tiles of 128 tokens
-    assert f(4, 8, 8, 64, 129) == slots                 # 8 KV heads: the same
+    assert f(4, 8, 8, 64, 129) == slots                 # 8 KV heads: head pairs, the same slots
     assert f(8, 32, 8, 128, 131072) == max(8 * 32 * 512 * 130 * 4, slots)
     assert f(1, 6, 4, 128, 4096) == 0                   # 6 % 4 != 0
     assert f(1, 8, 8, 96, 4096) == 0                    # head_dim unsupported
@@ -104,6 +104,23 @@ def test_decode_host_validation(lib):
     if not torch.cuda.is_available():
         assert _decode(lib) == -7                            # valid, but no device here
         assert _decode(lib, mb=64, msl=1024, ws=NULL) == -4  # needs split-K scratch
+
+
+def test_selftest_host_validation(lib):
+    f = lib.pk_selftest_decode_wait_timeout
+
+    def call(stall=1, limit_us=5000, **kw):
+        a = dict(out=_fake(), dt=0, q=_fake(), kc=_fake(), vc=_fake(), bt=_fake(), mb=4, sl=_fake(), msl=64,
+                 n=2, h=8, hkv=2, d=128, nb=16, b=16, scale=0.088, ws=_fake(), wsb=1 << 30)
+        a.update(kw)
+        return f(a["out"], a["dt"], a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"], a["msl"], a["n"], a["h"],
+                 a["hkv"], a["d"], a["nb"], a["b"], a["scale"], a["ws"], a["wsb"], stall, limit_us, None)
+    assert call(stall=0) == -2 and call(stall=-3) == -2       # a stall must name a tile >= 1
+    assert call(limit_us=50) == -2 and call(limit_us=2000000) == -2
+    assert call(d=96) == -3                                   # then the decode call's own checks
+    assert call(n=0) == 0
+    if not torch.cuda.is_available():
+        assert call() == -7
 
 
 def test_cache_ops_host_validation(lib):

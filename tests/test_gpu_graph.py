@@ -33,8 +33,8 @@ def test_decode_step_replays_in_a_cuda_graph():
     w = W.get("prefix-b16", 0)
     t = W.make_tensors(w, DEV)
     assert t["copy_pairs"].shape[0] > 0 and w.num_new_tokens > 0
-    ws = torch.empty(max(1, pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
-                                                         w.max_seq_len)), dtype=torch.uint8, device=DEV)
+    ws = pk.new_workspace((pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                         w.max_seq_len)), DEV)
     out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=DEV)
 
     def step():
