@@ -6,7 +6,13 @@ One step = one pass of the whole hot path over one batch: reshape_and_cache of
 the step's new tokens, copy_blocks of its copy-on-write pairs (prefix
 workloads only), then paged_attention_decode.  ``value`` is the step's useful
 bytes (attended K/V + Q + O + appended K/V read and written + copied blocks)
-over its device time, all inputs resident in HBM.  ``e2e`` is the same metric
+over its device time, all inputs resident in HBM.  When a step's K/V is at
+least twice the L2 (the Llama-3-70B batch reads 1.1 GB, 8.6x the L2), the K
+timed steps run back to back as in serving, alternating between two separate
+copies of the cache so that no step finds the previous step's reads in L2,
+with one pair of CUDA events around them; smaller workloads flush L2 before
+each step and time each step with its own events.  ``isolated_call`` adds the
+decode call timed alone with L2 flushed.  ``e2e`` is the same metric
 through the public API with per-step inputs (q, new K/V, slots, tables,
 lengths) copied from pinned host memory and the output copied back inside the
 timed region; the KV cache itself stays resident, as it does in serving.
@@ -178,8 +184,10 @@ N, B, K = w.num_seqs, w.block_size, {steps}
 lens = [int(x) for x in w.seq_lens]
 MB = -(-(max(lens) + K) // B)
 ids = np.arange(N, dtype=np.int64)
+# Every sequence gets private blocks here (no prefix sharing): size the pool for that.
+POOL = sum(-(-(L + K) // B) for L in lens) + N
 def native():
-    bm = BlockManager(w.num_blocks + N * (K // B + 2), B)
+    bm = BlockManager(POOL, B)
     for s in range(N):
         bm.add_sequence(s)
         bm.append_slots(np.full(lens[s], s, dtype=np.int64))
@@ -192,7 +200,7 @@ def native():
     return ts
 def reference():
     import oracle
-    bm = oracle.CowBlockManager(w.num_blocks + N * (K // B + 2), B)
+    bm = oracle.CowBlockManager(POOL, B)
     for s in range(N):
         bm.new_sequence(str(s))
         for _ in range(lens[s]):
@@ -342,15 +350,18 @@ def aggregate_over_ranks(device_ms: float, e2e_ms: float, step_bytes: float, dev
 
 def contiguous_tables(w):
     """Block tables of the same lengths with every sequence's blocks back to
-    back (bt[s, i] = base_s + i): the paging-overhead control layout."""
+    back (bt[s, i] = base_s + i): the paging-overhead control layout.  None
+    when the pool is too small for it (a workload whose sequences share
+    blocks holds fewer blocks than its sequences' lengths add up to)."""
     import numpy as np
     bt = np.full_like(w.block_tables, -1)
     base = 0
     for s in range(w.num_seqs):
         nb = -(-int(w.seq_lens[s]) // w.block_size)
+        if base + nb > w.num_blocks:
+            return None
         bt[s, :nb] = np.arange(base, base + nb, dtype=np.int32)
         base += nb
-    assert base <= w.num_blocks
     return bt
 
 
@@ -409,7 +420,32 @@ def workload_report(name, seed, dev, steps, flush, peak):
     ms = time_decode(fn, steps, flush, stream)
     gbs = ub["attention"] / (ms * 1e-3) / 1e9
     rep = {"decode_ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-           "tokens_per_s_per_layer": round(w.num_seqs / (ms * 1e-3), 1)}
+           "tokens_per_s_per_layer": round(w.num_seqs / (ms * 1e-3), 1),
+           "timing": "one call at a time, L2 flushed before each"}
+    if ub["kv_unique"] >= 2 * torch.cuda.get_device_properties(dev).L2_cache_size:
+        # Back to back, alternating between two copies of the cache (as the
+        # bench line's steps run).
+        kc2, vc2 = t["k_cache"].clone(), t["v_cache"].clone()
+        pairs = [(t["k_cache"], t["v_cache"]), (kc2, vc2)]
+
+        def fn2(i):
+            pk.pk_paged_attention_decode(out, t["q"], pairs[i & 1][0], pairs[i & 1][1], t["block_tables"],
+                                         t["seq_lens"], w.scale, w.block_size, w.max_seq_len, ws)
+        for i in range(4):
+            fn2(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n2 = max(steps, 100)
+        a.record(stream)
+        for i in range(n2):
+            fn2(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms2 = a.elapsed_time(b) / n2
+        gbs2 = ub["attention"] / (ms2 * 1e-3) / 1e9
+        rep["back_to_back"] = {"decode_ms": round(ms2, 4), "gbs": round(gbs2, 1), "frac": round(gbs2 / peak, 4),
+                               "tokens_per_s_per_layer": round(w.num_seqs / (ms2 * 1e-3), 1),
+                               "timing": f"{n2} calls back to back alternating between two copies of the cache"}
+        del kc2, vc2, pairs
     # The cache writes alone (each call repeats the same copies and writes, so
     # it is idempotent); GB/s of bytes read plus written.
     if w.copy_pairs.shape[0]:
@@ -635,15 +671,26 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flush = L2Flush(dev)
 
-    def attend(o=out, q=t["q"], bt=t["block_tables"], sl=t["seq_lens"]):
-        pk.pk_paged_attention_decode(o, q, t["k_cache"], t["v_cache"], bt, sl, w.scale, w.block_size,
-                                     w.max_seq_len, workspace)
+    # When a step's K/V is far larger than L2, steps run back to back as in
+    # serving, with no flush: consecutive steps use two separate copies of the
+    # cache (two layers of the model), so nothing a step reads was left in L2
+    # by the step before.  Smaller workloads flush L2 before every step.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream_mode = ub["kv_unique"] >= 2 * l2_bytes
+    caches = [(t["k_cache"], t["v_cache"])]
+    if stream_mode:
+        caches.append((t["k_cache"].clone(), t["v_cache"].clone()))
 
-    def prelude(kn=t["k_new"], vn=t["v_new"], sm=t["slot_mapping"]):
+    def attend(o=out, q=t["q"], bt=t["block_tables"], sl=t["seq_lens"], c=0):
+        kc, vc = caches[c % len(caches)]
+        pk.pk_paged_attention_decode(o, q, kc, vc, bt, sl, w.scale, w.block_size, w.max_seq_len, workspace)
+
+    def prelude(kn=t["k_new"], vn=t["v_new"], sm=t["slot_mapping"], c=0):
+        kc, vc = caches[c % len(caches)]
         if w.copy_pairs.shape[0]:
-            pk.copy_blocks(t["k_cache"], t["v_cache"], t["copy_pairs"])
+            pk.copy_blocks(kc, vc, t["copy_pairs"])
         if w.num_new_tokens:
-            pk.reshape_and_cache(kn, vn, t["k_cache"], t["v_cache"], sm)
+            pk.reshape_and_cache(kn, vn, kc, vc, sm)
 
     # Launches of this library per step: copy, append, then the decode kernel
     # and its merge (the merge runs when a sequence can span several CTAs /
@@ -654,30 +701,67 @@ def run_ours(args):
     merge = w.max_seq_len > (128 if tensor_core else 512)
     launches_per_step = (1 if w.copy_pairs.shape[0] else 0) + (1 if w.num_new_tokens else 0) + 1 + (1 if merge else 0)
 
-    for _ in range(args.warmup):
-        prelude()
-        attend()
+    for i in range(args.warmup):
+        prelude(c=i)
+        attend(c=i)
     torch.cuda.synchronize(dev)
     assert pk.pk_get_device_error(dev) == 0
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    timed_launches = launches_per_step * args.steps
     with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            flush()                                           # cold, clean L2 between steps (outside the events)
-            ev[i][0].record(stream)
-            prelude()
-            ev[i][1].record(stream)
-            attend()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize(dev)
+        if stream_mode:
+            # The K timed steps back to back, one pair of events around them;
+            # then the decode call alone the same way (the roofline's launch
+            # duration).
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush()
+            e0.record(stream)
+            for i in range(args.steps):
+                prelude(c=i)
+                attend(c=i)
+            e1.record(stream)
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for i in range(args.steps):
+                attend(c=i)
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            total_ms = e0.elapsed_time(e1)
+            attn_avg_ms = a0.elapsed_time(a1) / args.steps
+            timed_launches += (1 + (1 if merge else 0)) * args.steps
+        else:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+            for i in range(args.steps):
+                flush()                                       # cold, clean L2 between steps (outside the events)
+                ev[i][0].record(stream)
+                prelude()
+                ev[i][1].record(stream)
+                attend()
+                ev[i][2].record(stream)
+            torch.cuda.synchronize(dev)
+            total_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
+            attn_avg_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
         if ws > 1:
             torch.distributed.barrier()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    total_ms = sum(step_ms)
+    assert pk.pk_get_device_error(dev) == 0
+
+    # One call at a time with L2 cold and clean before each (context, and the
+    # cache writes' own time).
+    iso_steps = max(10, min(args.steps, 200))
+    iso = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iso_steps)]
+    for i in range(iso_steps):
+        flush()
+        iso[i][0].record(stream)
+        prelude()
+        iso[i][1].record(stream)
+        attend()
+        iso[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    iso_attn_ms = [e[1].elapsed_time(e[2]) for e in iso]
+    iso_pre_ms = [e[0].elapsed_time(e[1]) for e in iso]
 
     # End to end through the public API with host buffers, as a serving loop
     # runs it: every step copies its inputs from pinned host memory and reads
@@ -705,8 +789,8 @@ def run_ours(args):
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])           # step i-2's output has been read back
-        prelude(dbufs[b]["k_new"], dbufs[b]["v_new"], dbufs[b]["slot_mapping"])
-        attend(outs[b], dbufs[b]["q"], dbufs[b]["block_tables"], dbufs[b]["seq_lens"])
+        prelude(dbufs[b]["k_new"], dbufs[b]["v_new"], dbufs[b]["slot_mapping"], c=i)
+        attend(outs[b], dbufs[b]["q"], dbufs[b]["block_tables"], dbufs[b]["seq_lens"], c=i)
         ev_done[b].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_done[b])
@@ -734,10 +818,13 @@ def run_ours(args):
     assert torch.equal(out_hosts[(args.steps - 1) & 1], outs[(args.steps - 1) & 1].cpu())
 
     # Paging-overhead control: the same kernel and lengths, contiguous tables.
-    bt_contig = torch.from_numpy(contiguous_tables(w)).to(dev)
+    contig = contiguous_tables(w)
     ctl_steps = max(10, min(args.steps, 100))
     paged_ms = time_decode(lambda: attend(), ctl_steps, flush, stream)
-    contig_ms = time_decode(lambda: attend(bt=bt_contig), ctl_steps, flush, stream)
+    contig_ms = None
+    if contig is not None:
+        bt_contig = torch.from_numpy(contig).to(dev)
+        contig_ms = time_decode(lambda: attend(bt=bt_contig), ctl_steps, flush, stream)
     assert pk.pk_get_device_error(dev) == 0
 
     others = {}
@@ -767,8 +854,18 @@ def run_ours(args):
     peak, peak_kind = load_peaks()
     ms_per_step = total_ms / args.steps
     value = all_bytes * args.steps / (total_ms * 1e-3) / 1e9
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
     attn_gbs = ub["attention"] / (attn_avg_ms * 1e-3) / 1e9
+    iso_ms = statistics.median(iso_attn_ms)
+    if stream_mode:
+        l2_note = (f"inputs larger than L2: each step reads {ub['kv_unique'] / 1e9:.2f} GB of K/V "
+                   f"({ub['kv_unique'] / l2_bytes:.1f}x the {l2_bytes / 1e6:.0f} MB L2) from one of two separate "
+                   "caches used alternately (two layers), so nothing a step reads was left in L2 by the step "
+                   "before; the K steps run back to back with no flush, one pair of CUDA events around them "
+                   "(L2 flushed once before the first); the roofline's launch duration comes from K decode "
+                   "calls timed the same way")
+    else:
+        l2_note = ("flushed between timed steps outside the events (256 MiB write, then a 256 MiB read so that "
+                   "the write's dirty lines are written back before the step)")
     traffic = None
     if (RECORDED_TRAFFIC["sources_sha1"] == sources_sha1() and RECORDED_TRAFFIC["workload"] == args.workload
             and not args.shape):
@@ -796,8 +893,7 @@ def run_ours(args):
             "copy_pairs": int(w.copy_pairs.shape[0]), "seed": args.seed,
             "useful_bytes_per_step": ub["step"], "attention_bytes": ub["attention"],
             "unique_kv_bytes": ub["kv_unique"],
-            "l2": "flushed between timed steps outside the events (256 MiB write, then a 256 MiB read so that "
-                  "the write's dirty lines are written back before the step); K/V inputs also exceed L2",
+            "l2": l2_note,
             "parallelism": f"replicas x{ws} (independent batches, no collective)",
             "decode_path": args.decode_path,
         },
@@ -826,20 +922,30 @@ def run_ours(args):
         },
         "paging_overhead": {
             "paged_decode_ms": round(paged_ms, 5),
-            "contiguous_decode_ms": round(contig_ms, 5),
-            "overhead": round(paged_ms / contig_ms - 1.0, 4),
+            "contiguous_decode_ms": round(contig_ms, 5) if contig_ms else None,
+            "overhead": round(paged_ms / contig_ms - 1.0, 4) if contig_ms else None,
+            "skipped": None if contig_ms else "the sequences share blocks: laid out back to back they would need "
+                                             "more blocks than the pool holds",
             "note": "same kernel and lengths with bt[s, i] = base_s + i; the pages quote a 20-26% kernel "
                     "slowdown vs a contiguous kernel for the 2023 paged kernel (context, not a target)",
         },
-        "gpu_launches": launches_per_step * args.steps,
+        "isolated_call": {
+            "decode_ms": round(iso_ms, 5),
+            "gbs": round(ub["attention"] / (iso_ms * 1e-3) / 1e9, 1),
+            "frac": round(ub["attention"] / (iso_ms * 1e-3) / 1e9 / peak, 4),
+            "what": f"one decode call at a time, L2 cold and clean before each (256 MiB write + read), CUDA "
+                    f"events around the call, median of {iso_steps} (no overlap with a neighbouring launch)",
+        },
+        "gpu_launches": timed_launches,
         "clocks": clocks.summary(),
     }
     pre_bytes = ub["append"] + ub["copies"]
-    pre_ms = statistics.median([e[0].elapsed_time(e[1]) for e in ev])
+    pre_ms = statistics.median(iso_pre_ms)
     if pre_bytes > 0 and pre_ms > 0:
         res["cache_ops"] = {
-            "what": "copy_blocks (the copy-on-write pairs, if any) then reshape_and_cache of each timed step, "
-                    "between the same events (L2 cold before each step); bytes read plus written",
+            "what": "copy_blocks (the copy-on-write pairs, if any) then reshape_and_cache of a step, between "
+                    "their own events (L2 cold before each step, median of the isolated steps); bytes read "
+                    "plus written",
             "us_per_step": round(pre_ms * 1e3, 2),
             "bytes_per_step": pre_bytes,
             "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
