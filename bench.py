@@ -1053,6 +1053,9 @@ def main():
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill workload (16 x 512-token chunks over 4096 earlier tokens) "
                          "and print its report; a small case for profiling the prefill kernel")
+    ap.add_argument("--multi-query-only", action="store_true",
+                    help="time only the speculative-verification workload (the workload's sequences, 2 newest "
+                         "tokens each as causal queries) and print its report; a case for profiling")
     ap.add_argument("--shape", default="",
                     help="H:Hkv:D -- the workload's sequence lengths with these head counts and head dim "
                          "(attention only; for kernel comparisons such as small groups or head dim 64)")
@@ -1071,6 +1074,16 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         print(json.dumps({"prefill": prefill_report(dev, L2Flush(dev), steps=args.steps)}), flush=True)
+        return
+    if args.multi_query_only:
+        import torch
+        from paged_kv_cache_122_gb300 import workloads as W
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        w = W.get(args.workload, args.seed)
+        t = W.make_tensors(w, dev)
+        rep = multi_query_report(w, t, dev, L2Flush(dev), load_peaks()[0], steps=args.steps)
+        print(json.dumps({"multi_query": rep}), flush=True)
         return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:

@@ -75,6 +75,21 @@ def test_head_dim_64_with_small_and_large_blocks(G, B, decode_path):
 
 
 @pytest.mark.parametrize("decode_path", PATHS, indirect=True)
+@pytest.mark.parametrize("Hkv,G", [(1, 4), (3, 2), (8, 1), (8, 4), (8, 8), (6, 16)])
+def test_head_dim_64_head_pairs_and_odd_kv_head_counts(Hkv, G, decode_path):
+    # At head dim 64 the tensor-core kernel reads two adjacent KV heads per
+    # tile when the KV head count is even and G <= 8; an odd count, or G = 16,
+    # keeps one head per tile.  Both must give the oracle's result, with
+    # sequences cut across CTAs.
+    w = W.custom(8, [1, 17, 129, 700, 2100, 4097], G * Hkv, Hkv, 64, 16)
+    t = W.make_tensors(w, DEV)
+    for dt in (torch.float32, torch.bfloat16):
+        out = _attend(w, t, dt)
+        assert_close(out.float().cpu().numpy(), _ref(w, t), dt == torch.bfloat16, f"Hkv={Hkv} G={G} D=64")
+    assert pk.pk_get_device_error() == 0
+
+
+@pytest.mark.parametrize("decode_path", PATHS, indirect=True)
 def test_physical_relabelling_gives_identical_bits(decode_path):
     w = W.custom(5, [3, 300, 1000, 2500], 32, 8, 128, 16)
     t = W.make_tensors(w, DEV)
