@@ -66,6 +66,44 @@ def test_decode_step_replays_in_a_cuda_graph():
     assert pk.pk_get_device_error() == 0
 
 
+def test_head_pair_decode_and_verification_replay_in_a_cuda_graph():
+    # Head dim 64 (tiles of two KV heads) and two newest tokens per sequence
+    # as causal queries on the decode kernel's columns, both with sequences
+    # cut across CTAs, captured together and replayed.
+    w = W.custom(43, [5, 300, 1500, 4000, 129, 2200], 32, 8, 64, 16)
+    t = W.make_tensors(w, DEV)
+    ws = pk.new_workspace(pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                       w.max_seq_len), DEV)
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float32, device=DEV)
+    N = w.num_seqs
+    cu = torch.arange(N + 1, dtype=torch.int32, device=DEV) * 2
+    gen = torch.Generator(device=DEV).manual_seed(11)
+    q2 = torch.randn(2 * N, w.num_heads, w.head_dim, generator=gen, device=DEV).to(torch.bfloat16)
+    out2 = torch.empty_like(q2)
+    ws2 = pk.new_workspace(pk.pk_decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                        w.max_seq_len), DEV)
+
+    def step():
+        pk.pk_paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"],
+                                     w.scale, w.block_size, w.max_seq_len, ws)
+        pk.paged_attention_multi_query(q2, cu, 2, t["k_cache"], t["v_cache"], t["block_tables"], t["seq_lens"],
+                                       w.scale, out=out2, max_seq_len=w.max_seq_len, workspace=ws2)
+
+    step()
+    torch.cuda.synchronize()
+    eager, eager2 = out.clone(), out2.clone()
+    g = _capture(step)
+    out.zero_()
+    out2.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager) and torch.equal(out2, eager2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager) and torch.equal(out2, eager2)
+    assert pk.pk_get_device_error() == 0
+
+
 def test_prompt_chunk_replays_in_a_cuda_graph():
     # The prefill kernel (two query tiles per CTA) under capture.
     lens = [300, 1111]
