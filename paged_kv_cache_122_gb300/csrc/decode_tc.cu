@@ -145,10 +145,13 @@ struct Walk {
 // The flattened (sequence, KV head, tile) space is cut into ranges of equal
 // cost, not of equal tile count: a CTA's time grows with the (sequence,
 // KV head) segments in its range (each loads its queries, sets up and reads
-// out its O) as well as with its tiles -- measured on the Llama-3-70B-shaped
-// batch, about 0.29 of a tile per segment.
+// out its O) as well as with its tiles.  Measured per CTA with in-kernel
+// timestamps on the Llama-3-70B length mix: a segment costs about 0.36 of a
+// tile when at most 8 query columns are in use, and about 1.4 tiles with 16
+// (the read-out and the reference-max moves work on every column).
 constexpr int64_t kTileCost = 7;
-constexpr int64_t kSegCost = 2;
+template <int NUSED>
+constexpr int64_t seg_cost() { return NUSED > 8 ? 10 : 2; }
 
 // Warp max of a float in one integer reduction: the bits are mapped to an
 // unsigned key with the same order (a non-negative float gets its sign bit
@@ -192,6 +195,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     constexpr uint32_t kTmemCols = HP == 2 ? 128 : 64;
     constexpr int CW = HP == 2 ? 8 : kNPad;           // P columns per head of the tile
     constexpr int NCOL = HP == 2 ? 8 + NC : NC;       // columns 0 .. NCOL-1 may be in use
+    constexpr int64_t kSegCost = seg_cost<HP * NC>();   // a segment's cost (the columns in use), in 1/7 tiles
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
