@@ -41,9 +41,11 @@
 //           segment's O is read out of TMEM one tile after its last P.V was
 //           issued, normalised and stored (or written to a slot if cut).
 // Launch: the decode grid is a programmatic dependent of the previous kernel
-// in the stream (its set-up overlaps that kernel's tail; it touches global
-// memory only after it completed), and the merge grid is a programmatic
-// dependent of the decode grid.
+// in the stream (its set-up overlaps that kernel's tail; before that kernel
+// has completed it touches global memory only with L2 prefetches), and the
+// merge grid is a programmatic dependent of the decode grid.  The merge grid
+// lets the next decode grid start at once, so back-to-back calls overlap one
+// call's set-up with the previous call's end.
 // Query heads are padded to the MMA's N = 16; padded columns are ignored.
 #include "decode.cuh"
 #include "sm100.cuh"
@@ -71,6 +73,7 @@ constexpr uint32_t kQChunkBytes = kNPad * 128;
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + 2 * kQChunkBytes;
 constexpr uint32_t kPBytes = kTile * kNPad * 2;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s: far beyond any legal wait (default)
+constexpr int kLenCache = 2048;                              // lengths kept in shared memory up to this batch
 
 constexpr uint32_t kIdescQK = idesc_bf16(kTile, kNPad, 0, 0);   // A = K (K-major), B = Q (K-major)
 constexpr uint32_t kIdescPV = idesc_bf16(128, kNPad, 1, 1);     // A = V^T (MN-major), B = P^T (MN-major)
@@ -98,6 +101,7 @@ struct Misc {
     int4 qmeta[kStages];           // (first query row, query tokens, first query position, 0) of it
     float red[4][kNPad];          // per-warp maxima when the reference max moves
     float lsum[4][kNPad];
+    int lens[kLenCache];          // the raw sequence lengths, when num_seqs <= kLenCache
 };
 
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 2 * kPBytes + sizeof(Misc);
@@ -118,26 +122,43 @@ struct Slot {
 };
 constexpr size_t kMaxCtas = kTcMaxCtas;
 
-__device__ __forceinline__ int clamp_len(const DecodeParams &p, int s, int cap) {
-    const int raw = p.seq_lens[s];
-    return raw < 0 ? 0 : (raw > cap ? cap : raw);
+// A 32-bit load that bypasses L1: L2 is coherent with writes of other
+// grids, so a value read before the programmatic wait and read again after
+// it cannot come back stale from L1.
+__device__ __forceinline__ int ld_cg(const int *p) {
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
 }
+
+// The sequence lengths, from the shared-memory copy when there is one;
+// operator() clamps to [0, cap] (values outside are reported separately).
+struct LenSrc {
+    const int *cache;   // shared memory, or null
+    const int *glob;
+    int cap;
+    __device__ __forceinline__ int raw(int s) const { return cache ? cache[s] : glob[s]; }
+    __device__ __forceinline__ int operator()(int s) const {
+        const int r = raw(s);
+        return r < 0 ? 0 : (r > cap ? cap : r);
+    }
+};
 
 // Walks the flattened (sequence, KV head group, tile) space in order.
 struct Walk {
-    int s, h, t, nt, L, nh;          // nh: KV head groups per sequence
-    __device__ __forceinline__ void load(const DecodeParams &p, int cap) {
-        L = clamp_len(p, s, cap);
+    int s, h, t, nt, L, nh, ns;      // nh: KV head groups per sequence; ns: sequences
+    __device__ __forceinline__ void load(const LenSrc &len) {
+        L = len(s);
         nt = (L + kTile - 1) / kTile;
     }
-    __device__ __forceinline__ void next(const DecodeParams &p, int cap) {
+    __device__ __forceinline__ void next(const LenSrc &len) {
         if (++t < nt) return;
         t = 0;
         if (++h < nh) return;
         h = 0;
         do {
-            if (++s >= p.num_seqs) return;
-            load(p, cap);
+            if (++s >= ns) return;
+            load(len);
         } while (nt == 0);
     }
 };
@@ -150,6 +171,9 @@ struct Walk {
 // tile when at most 8 query columns are in use, and about 1.4 tiles with 16
 // (the read-out and the reference-max moves work on every column).
 constexpr int64_t kTileCost = 7;
+// Block tables up to this size are brought into L2 (split over the CTAs)
+// while the previous grid in the stream finishes.
+constexpr size_t kTablePrefetchBytes = size_t{8} << 20;
 template <int NUSED>
 constexpr int64_t seg_cost() { return NUSED > 8 ? 10 : 2; }
 
@@ -246,106 +270,194 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_q);
     }
-    // Launched as a programmatic dependent of the previous kernel in the
-    // stream: everything above overlaps its tail; no global memory is touched
-    // before it has completed.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x == 0 && slots) slots[2 * c].flag = 0;
-    // The merge grid may start now; it waits for this grid's completion.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (warp == 2 && lane == 0) {
+        // The set-up below reads the lengths, then the block tables: have L2
+        // fetch them (this CTA's share of the tables) now.  A prefetch
+        // brings nothing into the CTA, and L2 stays coherent with whatever
+        // the previous grid still writes.
+        prefetch_l2_span(p.seq_lens, 0, static_cast<size_t>(N) * 4);
+        if constexpr (MQ) prefetch_l2_span(p.cu_q_lens, 0, static_cast<size_t>(N + 1) * 4);
+        const size_t tb = static_cast<size_t>(N) * p.max_blocks_per_seq * 4;
+        if (tb <= kTablePrefetchBytes)
+            prefetch_l2_span(p.block_tables, tb * c / C, tb * (c + 1) / C);
+    }
 
     // ---- this CTA's range of the flattened tile space ----------------------
     // Tile x (its cost interval starting at a_x: a segment's tile 0 covers
     // [start, start + kSegCost + kTileCost), tile t >= 1 starts at start +
     // kSegCost + kTileCost * t) belongs to CTA k when P_k <= a_x < P_{k+1},
-    // P_k = k * W / C, W the total cost.
+    // P_k = k * W / C, W the total cost.  plan() finds it from the lengths
+    // (every thread calls it); it returns, for the whole CTA, whether some
+    // length is zero or outside [0, cap].
+    const bool cached = N <= kLenCache;
+    const LenSrc lens{cached ? misc->lens : nullptr, p.seq_lens, cap};
     const int per = (N + kThreads - 1) / kThreads;
     const int s_lo = min(N, static_cast<int>(threadIdx.x) * per), s_hi = min(N, s_lo + per);
-    int64_t mine = 0, mine_w = 0;
-    for (int s = s_lo; s < s_hi; ++s) {
-        const int raw = p.seq_lens[s];
-        if ((raw < 0 || raw > cap) && s % C == c) set_error(p.err, PK_DEVERR_SEQ_LEN);
-        const int L = raw < 0 ? 0 : (raw > cap ? cap : raw);
-        const int64_t nt = (L + kTile - 1) / kTile;
-        mine += nt * Hkv;
-        mine_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
-    }
-    int64_t T, W;
-    const int64_t my_off = block_exclusive_scan<kThreads>(mine, misc->scan, &T);
-    const int64_t my_off_w = block_exclusive_scan<kThreads>(mine_w, misc->scan_w, &W);
-    for (int k = 0; k < 2; ++k) {
-        const int64_t P = static_cast<int64_t>(c + k) * W / C;
-        if (P >= W) {
-            if (threadIdx.x == 0) misc->bnd[k] = T;
-            continue;
+    int64_t T = 0, W = 0;
+    auto plan = [&]() -> int {
+        int64_t mine = 0, mine_w = 0;
+        int odd = 0;
+        for (int s = s_lo; s < s_hi; ++s) {
+            const int raw = lens.raw(s);
+            odd |= raw <= 0 || raw > cap;
+            const int64_t nt = (lens(s) + kTile - 1) / kTile;
+            mine += nt * Hkv;
+            mine_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
         }
-        if (my_off_w <= P && P < my_off_w + mine_w) {
-            int64_t acc_t = my_off, acc_w = my_off_w;
-            for (int s = s_lo; s < s_hi; ++s) {
-                const int64_t nt = (clamp_len(p, s, cap) + kTile - 1) / kTile;
-                const int64_t segc = kTileCost * nt + kSegCost;
-                const int64_t cw = nt > 0 ? segc * Hkv : 0;
-                if (P < acc_w + cw) {
-                    const int64_t q = P - acc_w;
-                    int64_t h = q / segc;
-                    const int64_t r = q - h * segc;
-                    // The first tile of the segment that starts at or after r.
-                    int64_t t = r == 0 ? 0 : (r - kSegCost + kTileCost - 1) / kTileCost;
-                    if (r > 0 && t < 1) t = 1;
-                    if (t >= nt) {
-                        ++h;
-                        t = 0;
+        const int64_t my_off = block_exclusive_scan<kThreads>(mine, misc->scan, &T);
+        const int64_t my_off_w = block_exclusive_scan<kThreads>(mine_w, misc->scan_w, &W);
+        for (int k = 0; k < 2; ++k) {
+            const int64_t P = static_cast<int64_t>(c + k) * W / C;
+            if (P >= W) {
+                if (threadIdx.x == 0) misc->bnd[k] = T;
+                continue;
+            }
+            if (my_off_w <= P && P < my_off_w + mine_w) {
+                int64_t acc_t = my_off, acc_w = my_off_w;
+                for (int s = s_lo; s < s_hi; ++s) {
+                    const int64_t nt = (lens(s) + kTile - 1) / kTile;
+                    const int64_t segc = kTileCost * nt + kSegCost;
+                    const int64_t cw = nt > 0 ? segc * Hkv : 0;
+                    if (P < acc_w + cw) {
+                        const int64_t q = P - acc_w;
+                        int64_t h = q / segc;
+                        const int64_t r = q - h * segc;
+                        // The first tile of the segment that starts at or after r.
+                        int64_t t = r == 0 ? 0 : (r - kSegCost + kTileCost - 1) / kTileCost;
+                        if (r > 0 && t < 1) t = 1;
+                        if (t >= nt) {
+                            ++h;
+                            t = 0;
+                        }
+                        misc->bnd[k] = acc_t + h * nt + t;
+                        break;
                     }
-                    misc->bnd[k] = acc_t + h * nt + t;
-                    break;
+                    acc_t += nt * Hkv;
+                    acc_w += cw;
                 }
-                acc_t += nt * Hkv;
-                acc_w += cw;
+            }
+        }
+        __syncthreads();
+        const int64_t b0 = misc->bnd[0];
+        if (misc->bnd[1] > b0) {
+            int64_t acc = my_off, acc_w = my_off_w;
+            if (acc <= b0 && b0 < acc + mine) {
+                for (int s = s_lo; s < s_hi; ++s) {
+                    const int64_t nt = (lens(s) + kTile - 1) / kTile;
+                    const int64_t w = nt * Hkv;
+                    if (b0 < acc + w) {
+                        misc->s0 = s;
+                        misc->rem0 = b0 - acc;
+                        // If the range starts inside a segment, the CTA where that
+                        // segment starts (the owner of its tile 0's cost start).
+                        const int64_t h0 = (b0 - acc) / nt;
+                        const int64_t a = acc_w + h0 * (kTileCost * nt + kSegCost);
+                        int64_t k = W > 0 ? a * C / W : 0;
+                        while (k + 1 < C && (k + 1) * W / C <= a) ++k;
+                        while (k > 0 && k * W / C > a) --k;
+                        misc->first_cta = static_cast<int32_t>(k);
+                        break;
+                    }
+                    acc += w;
+                    acc_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
+                }
+            }
+        }
+        return __syncthreads_or(odd);
+    };
+    // The first tile of the range, from the plan.
+    auto first_tile = [&]() -> Walk {
+        Walk w{};
+        w.nh = Hkv;
+        w.ns = N;
+        w.s = misc->s0;
+        w.load(lens);
+        w.h = static_cast<int>(misc->rem0 / w.nt);
+        w.t = static_cast<int>(misc->rem0 % w.nt);
+        return w;
+    };
+
+    // With the lengths in shared memory, the plan is made before the wait,
+    // while the previous grid finishes, and the first tile's pages and
+    // queries are prefetched into L2 from block-table entries read ahead.
+    // After the wait the lengths are read again: the plan is redone only if
+    // one changed, and everything the CTA loads or stores is read afresh.
+    constexpr int kPerMax = (kLenCache + kThreads - 1) / kThreads;
+    int odd = 0;
+    if (cached) {
+        for (int s = threadIdx.x; s < N; s += kThreads) misc->lens[s] = ld_cg(p.seq_lens + s);
+        __syncthreads();
+        odd = plan();
+        if (warp == 0 && misc->bnd[1] > misc->bnd[0]) {
+            const Walk w = first_tile();
+            const int fp = w.t * kTile / B;
+            const int pages = (min(kTile, w.L - w.t * kTile) + B - 1) / B;
+            if (lane < pages && fp + lane < p.max_blocks_per_seq && p.num_blocks > 0) {
+                int phys = ld_cg(p.block_tables + static_cast<size_t>(w.s) * p.max_blocks_per_seq + fp + lane);
+                phys = phys < 0 ? 0 : (phys >= p.num_blocks ? p.num_blocks - 1 : phys);
+                tma_prefetch_5d(&tm_k, 0, 0, 0, phys * (B >> 3), w.h);
+                tma_prefetch_5d(&tm_v, 0, 0, 0, phys * (B >> 3), w.h);
+            }
+            if (!MQ && lane < NCH) {
+                const int qx = HP == 2 ? 0 : lane * 64;
+                const int qh = (w.h * HP + (HP == 2 ? lane : 0)) * Gq;
+                tma_prefetch_2d(&tm_q, qx, w.s * H + qh);
             }
         }
     }
-    __syncthreads();
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: everything above overlaps its tail; apart from L2 prefetches
+    // and reads that are checked below, no global memory is touched before
+    // it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0 && slots) slots[2 * c].flag = 0;
+    // The merge grid may start now; it waits for this grid's completion.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (cached) {
+        int fresh[kPerMax];
+        int changed = 0;
+#pragma unroll
+        for (int j = 0; j < kPerMax; ++j) {
+            const int s = static_cast<int>(threadIdx.x) + j * kThreads;
+            if (s < N) {
+                fresh[j] = ld_cg(p.seq_lens + s);
+                changed |= fresh[j] != misc->lens[s];
+            }
+        }
+        if (__syncthreads_or(changed)) {
+#pragma unroll
+            for (int j = 0; j < kPerMax; ++j) {
+                const int s = static_cast<int>(threadIdx.x) + j * kThreads;
+                if (s < N) misc->lens[s] = fresh[j];
+            }
+            __syncthreads();
+            odd = plan();
+        }
+    } else {
+        odd = plan();
+    }
     const int64_t beg = misc->bnd[0], end = misc->bnd[1];
     if (threadIdx.x == 0 && slots) slots[2 * c].range_beg = beg;
     const int n_tiles = static_cast<int>(end - beg);
-    if (n_tiles > 0) {
-        int64_t acc = my_off, acc_w = my_off_w;
-        if (acc <= beg && beg < acc + mine) {
-            for (int s = s_lo; s < s_hi; ++s) {
-                const int64_t nt = (clamp_len(p, s, cap) + kTile - 1) / kTile;
-                const int64_t w = nt * Hkv;
-                if (beg < acc + w) {
-                    misc->s0 = s;
-                    misc->rem0 = beg - acc;
-                    // If the range starts inside a segment, the CTA where that
-                    // segment starts (the owner of its tile 0's cost start).
-                    const int64_t h0 = (beg - acc) / nt;
-                    const int64_t a = acc_w + h0 * (kTileCost * nt + kSegCost);
-                    int64_t k = W > 0 ? a * C / W : 0;
-                    while (k + 1 < C && (k + 1) * W / C <= a) ++k;
-                    while (k > 0 && k * W / C > a) --k;
-                    misc->first_cta = static_cast<int32_t>(k);
-                    break;
-                }
-                acc += w;
-                acc_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
+    // Lengths outside [0, cap] are reported, and empty sequences get zeros,
+    // by CTA s % C.
+    if (odd || mq) {
+        for (int s = c; s < N; s += C) {
+            const int raw = lens.raw(s);
+            if ((raw < 0 || raw > cap) && threadIdx.x == 0) set_error(p.err, PK_DEVERR_SEQ_LEN);
+            const int L = lens(s);
+            if (mq) {
+                // A sequence has at most L query tokens (they are its newest tokens).
+                const int r0 = p.cu_q_lens[s], r1 = p.cu_q_lens[s + 1];
+                if (r1 < r0 || r1 - r0 > L) set_error(p.err, PK_DEVERR_SEQ_LEN);
+                if (L != 0) continue;
+                for (int64_t i = threadIdx.x; i < static_cast<int64_t>(max(r1 - r0, 0)) * H * D; i += kThreads)
+                    store_out(p, static_cast<size_t>(r0) * H * D + i, 0.f);
+                continue;
             }
-        }
-    }
-    // Empty sequences: zeros, written by CTA s % C.
-    for (int s = c; s < N; s += C) {
-        const int L = clamp_len(p, s, cap);
-        if (mq) {
-            // A sequence has at most L query tokens (they are its newest tokens).
-            const int r0 = p.cu_q_lens[s], r1 = p.cu_q_lens[s + 1];
-            if (r1 < r0 || r1 - r0 > L) set_error(p.err, PK_DEVERR_SEQ_LEN);
             if (L != 0) continue;
-            for (int64_t i = threadIdx.x; i < static_cast<int64_t>(max(r1 - r0, 0)) * H * D; i += kThreads)
-                store_out(p, static_cast<size_t>(r0) * H * D + i, 0.f);
-            continue;
+            for (int i = threadIdx.x; i < H * D; i += kThreads) store_out(p, static_cast<size_t>(s) * H * D + i, 0.f);
         }
-        if (L != 0) continue;
-        for (int i = threadIdx.x; i < H * D; i += kThreads) store_out(p, static_cast<size_t>(s) * H * D + i, 0.f);
     }
     tc_fence_before();
     __syncthreads();
@@ -354,12 +466,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     Walk w0{};
     w0.nh = Hkv;
-    if (n_tiles > 0) {
-        w0.s = misc->s0;
-        w0.load(p, cap);
-        w0.h = static_cast<int>(misc->rem0 / w0.nt);
-        w0.t = static_cast<int>(misc->rem0 % w0.nt);
-    }
+    w0.ns = N;
+    if (n_tiles > 0) w0 = first_tile();
 
     if (warp == 0) {
         // ================= producer =================
@@ -462,7 +570,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 tma_load_5d(sbase + kVOff + r0 * 128 * NCH, &tm_v, vfull, 0, 0, 0, rb, w.h);
             }
             ++issued;
-            w.next(p, cap);
+            w.next(lens);
             if (i + 1 < n_tiles) phys_next = fetch(w);
         }
         // On abort (or a self-test stall), let this warp's copies land before
@@ -843,6 +951,11 @@ template <int D, int NC, int HP>
 __global__ void __launch_bounds__(128)
 decode_tc_merge_kernel(const DecodeParams p, int C) {
     constexpr int CW = HP == 2 ? 8 : kNPad;
+    // A decode grid launched next in the stream as this grid's programmatic
+    // dependent may begin its set-up (it touches no global memory but L2
+    // prefetches before this grid completes).  Its CTAs find room only as
+    // this decode grid's CTAs leave their SMs.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the decode grid: wait for it
     // to finish and its writes to be visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
