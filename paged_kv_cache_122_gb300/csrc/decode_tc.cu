@@ -41,11 +41,12 @@
 //           segment's O is read out of TMEM one tile after its last P.V was
 //           issued, normalised and stored (or written to a slot if cut).
 // Launch: the decode grid is a programmatic dependent of the previous kernel
-// in the stream (its set-up overlaps that kernel's tail; before that kernel
-// has completed it touches global memory only with L2 prefetches), and the
-// merge grid is a programmatic dependent of the decode grid.  The merge grid
-// lets the next decode grid start at once, so back-to-back calls overlap one
-// call's set-up with the previous call's end.
+// in the stream: its set-up -- barriers, TMEM, and the plan of its range from
+// the sequence lengths (read again after the wait; the plan is redone if one
+// changed) -- overlaps that kernel's tail.  The merge grid is a programmatic
+// dependent of the decode grid and lets the next decode grid start at once,
+// so back-to-back calls overlap one call's set-up with the previous call's
+// end.
 // Query heads are padded to the MMA's N = 16; padded columns are ignored.
 #include "decode.cuh"
 #include "sm100.cuh"
@@ -163,6 +164,94 @@ struct Walk {
     }
 };
 
+// This CTA's range of the flattened tile space.  Tile x (its cost interval
+// starting at a_x: a segment's tile 0 covers [start, start + seg_cost +
+// kTileCost), tile t >= 1 starts at start + seg_cost + kTileCost * t)
+// belongs to CTA k when P_k <= a_x < P_{k+1}, P_k = k * W / C, W the total
+// cost.  Writes misc->bnd (the first tile of this range and of the next),
+// misc->s0 / rem0 (where the range starts) and misc->first_cta (the CTA in
+// whose range a segment cut at this range's start begins); returns the
+// total tile count and, in *odd, whether some length is zero or outside
+// [0, cap] (the same for every thread).  Every thread of the CTA calls it.
+template <int kThreadsT, typename MiscT>
+__device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, int N, int Hkv, int c, int C,
+                                           int64_t seg_cost, int tile_cost, int *odd) {
+    const int per = (N + kThreadsT - 1) / kThreadsT;
+    const int s_lo = min(N, static_cast<int>(threadIdx.x) * per), s_hi = min(N, s_lo + per);
+    const int cap = lens.cap;
+    int64_t mine = 0, mine_w = 0;
+    int bad = 0;
+    for (int s = s_lo; s < s_hi; ++s) {
+        const int raw = lens.raw(s);
+        bad |= raw <= 0 || raw > cap;
+        const int64_t nt = (lens(s) + kTile - 1) / kTile;
+        mine += nt * Hkv;
+        mine_w += nt > 0 ? (tile_cost * nt + seg_cost) * Hkv : 0;
+    }
+    int64_t T, W;
+    const int64_t my_off = block_exclusive_scan<kThreadsT>(mine, misc->scan, &T);
+    const int64_t my_off_w = block_exclusive_scan<kThreadsT>(mine_w, misc->scan_w, &W);
+    for (int k = 0; k < 2; ++k) {
+        const int64_t P = static_cast<int64_t>(c + k) * W / C;
+        if (P >= W) {
+            if (threadIdx.x == 0) misc->bnd[k] = T;
+            continue;
+        }
+        if (my_off_w <= P && P < my_off_w + mine_w) {
+            int64_t acc_t = my_off, acc_w = my_off_w;
+            for (int s = s_lo; s < s_hi; ++s) {
+                const int64_t nt = (lens(s) + kTile - 1) / kTile;
+                const int64_t segc = tile_cost * nt + seg_cost;
+                const int64_t cw = nt > 0 ? segc * Hkv : 0;
+                if (P < acc_w + cw) {
+                    const int64_t q = P - acc_w;
+                    int64_t h = q / segc;
+                    const int64_t r = q - h * segc;
+                    // The first tile of the segment that starts at or after r.
+                    int64_t t = r == 0 ? 0 : (r - seg_cost + tile_cost - 1) / tile_cost;
+                    if (r > 0 && t < 1) t = 1;
+                    if (t >= nt) {
+                        ++h;
+                        t = 0;
+                    }
+                    misc->bnd[k] = acc_t + h * nt + t;
+                    break;
+                }
+                acc_t += nt * Hkv;
+                acc_w += cw;
+            }
+        }
+    }
+    __syncthreads();
+    const int64_t b0 = misc->bnd[0];
+    if (misc->bnd[1] > b0) {
+        int64_t acc = my_off, acc_w = my_off_w;
+        if (acc <= b0 && b0 < acc + mine) {
+            for (int s = s_lo; s < s_hi; ++s) {
+                const int64_t nt = (lens(s) + kTile - 1) / kTile;
+                const int64_t w = nt * Hkv;
+                if (b0 < acc + w) {
+                    misc->s0 = s;
+                    misc->rem0 = b0 - acc;
+                    // If the range starts inside a segment, the CTA where that
+                    // segment starts (the owner of its tile 0's cost start).
+                    const int64_t h0 = (b0 - acc) / nt;
+                    const int64_t a = acc_w + h0 * (tile_cost * nt + seg_cost);
+                    int64_t k = W > 0 ? a * C / W : 0;
+                    while (k + 1 < C && (k + 1) * W / C <= a) ++k;
+                    while (k > 0 && k * W / C > a) --k;
+                    misc->first_cta = static_cast<int32_t>(k);
+                    break;
+                }
+                acc += w;
+                acc_w += nt > 0 ? (tile_cost * nt + seg_cost) * Hkv : 0;
+            }
+        }
+    }
+    *odd = __syncthreads_or(bad);
+    return T;
+}
+
 // The flattened (sequence, KV head, tile) space is cut into ranges of equal
 // cost, not of equal tile count: a CTA's time grows with the (sequence,
 // KV head) segments in its range (each loads its queries, sets up and reads
@@ -171,9 +260,6 @@ struct Walk {
 // tile when at most 8 query columns are in use, and about 1.4 tiles with 16
 // (the read-out and the reference-max moves work on every column).
 constexpr int64_t kTileCost = 7;
-// Block tables up to this size are brought into L2 (split over the CTAs)
-// while the previous grid in the stream finishes.
-constexpr size_t kTablePrefetchBytes = size_t{8} << 20;
 template <int NUSED>
 constexpr int64_t seg_cost() { return NUSED > 8 ? 10 : 2; }
 
@@ -270,101 +356,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_q);
     }
-    if (warp == 2 && lane == 0) {
-        // The set-up below reads the lengths, then the block tables: have L2
-        // fetch them (this CTA's share of the tables) now.  A prefetch
-        // brings nothing into the CTA, and L2 stays coherent with whatever
-        // the previous grid still writes.
-        prefetch_l2_span(p.seq_lens, 0, static_cast<size_t>(N) * 4);
-        if constexpr (MQ) prefetch_l2_span(p.cu_q_lens, 0, static_cast<size_t>(N + 1) * 4);
-        const size_t tb = static_cast<size_t>(N) * p.max_blocks_per_seq * 4;
-        if (tb <= kTablePrefetchBytes)
-            prefetch_l2_span(p.block_tables, tb * c / C, tb * (c + 1) / C);
-    }
-
     // ---- this CTA's range of the flattened tile space ----------------------
-    // Tile x (its cost interval starting at a_x: a segment's tile 0 covers
-    // [start, start + kSegCost + kTileCost), tile t >= 1 starts at start +
-    // kSegCost + kTileCost * t) belongs to CTA k when P_k <= a_x < P_{k+1},
-    // P_k = k * W / C, W the total cost.  plan() finds it from the lengths
-    // (every thread calls it); it returns, for the whole CTA, whether some
-    // length is zero or outside [0, cap].
+    // With the lengths in shared memory, the range is planned before the
+    // wait, while the previous grid in the stream finishes; after the wait
+    // the lengths are read again and the plan is redone only if one changed.
     const bool cached = N <= kLenCache;
     const LenSrc lens{cached ? misc->lens : nullptr, p.seq_lens, cap};
-    const int per = (N + kThreads - 1) / kThreads;
-    const int s_lo = min(N, static_cast<int>(threadIdx.x) * per), s_hi = min(N, s_lo + per);
-    int64_t T = 0, W = 0;
-    auto plan = [&]() -> int {
-        int64_t mine = 0, mine_w = 0;
-        int odd = 0;
-        for (int s = s_lo; s < s_hi; ++s) {
-            const int raw = lens.raw(s);
-            odd |= raw <= 0 || raw > cap;
-            const int64_t nt = (lens(s) + kTile - 1) / kTile;
-            mine += nt * Hkv;
-            mine_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
-        }
-        const int64_t my_off = block_exclusive_scan<kThreads>(mine, misc->scan, &T);
-        const int64_t my_off_w = block_exclusive_scan<kThreads>(mine_w, misc->scan_w, &W);
-        for (int k = 0; k < 2; ++k) {
-            const int64_t P = static_cast<int64_t>(c + k) * W / C;
-            if (P >= W) {
-                if (threadIdx.x == 0) misc->bnd[k] = T;
-                continue;
-            }
-            if (my_off_w <= P && P < my_off_w + mine_w) {
-                int64_t acc_t = my_off, acc_w = my_off_w;
-                for (int s = s_lo; s < s_hi; ++s) {
-                    const int64_t nt = (lens(s) + kTile - 1) / kTile;
-                    const int64_t segc = kTileCost * nt + kSegCost;
-                    const int64_t cw = nt > 0 ? segc * Hkv : 0;
-                    if (P < acc_w + cw) {
-                        const int64_t q = P - acc_w;
-                        int64_t h = q / segc;
-                        const int64_t r = q - h * segc;
-                        // The first tile of the segment that starts at or after r.
-                        int64_t t = r == 0 ? 0 : (r - kSegCost + kTileCost - 1) / kTileCost;
-                        if (r > 0 && t < 1) t = 1;
-                        if (t >= nt) {
-                            ++h;
-                            t = 0;
-                        }
-                        misc->bnd[k] = acc_t + h * nt + t;
-                        break;
-                    }
-                    acc_t += nt * Hkv;
-                    acc_w += cw;
-                }
-            }
-        }
-        __syncthreads();
-        const int64_t b0 = misc->bnd[0];
-        if (misc->bnd[1] > b0) {
-            int64_t acc = my_off, acc_w = my_off_w;
-            if (acc <= b0 && b0 < acc + mine) {
-                for (int s = s_lo; s < s_hi; ++s) {
-                    const int64_t nt = (lens(s) + kTile - 1) / kTile;
-                    const int64_t w = nt * Hkv;
-                    if (b0 < acc + w) {
-                        misc->s0 = s;
-                        misc->rem0 = b0 - acc;
-                        // If the range starts inside a segment, the CTA where that
-                        // segment starts (the owner of its tile 0's cost start).
-                        const int64_t h0 = (b0 - acc) / nt;
-                        const int64_t a = acc_w + h0 * (kTileCost * nt + kSegCost);
-                        int64_t k = W > 0 ? a * C / W : 0;
-                        while (k + 1 < C && (k + 1) * W / C <= a) ++k;
-                        while (k > 0 && k * W / C > a) --k;
-                        misc->first_cta = static_cast<int32_t>(k);
-                        break;
-                    }
-                    acc += w;
-                    acc_w += nt > 0 ? (kTileCost * nt + kSegCost) * Hkv : 0;
-                }
-            }
-        }
-        return __syncthreads_or(odd);
-    };
+    int64_t T = 0;
+    int odd = 0;
     // The first tile of the range, from the plan.
     auto first_tile = [&]() -> Walk {
         Walk w{};
@@ -376,65 +375,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         w.t = static_cast<int>(misc->rem0 % w.nt);
         return w;
     };
-
-    // With the lengths in shared memory, the plan is made before the wait,
-    // while the previous grid finishes, and the first tile's pages and
-    // queries are prefetched into L2 from block-table entries read ahead.
-    // After the wait the lengths are read again: the plan is redone only if
-    // one changed, and everything the CTA loads or stores is read afresh.
-    constexpr int kPerMax = (kLenCache + kThreads - 1) / kThreads;
-    int odd = 0;
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: what comes before the wait overlaps that kernel's tail.  Apart
+    // from the lengths, which are checked after it, no global memory is read
+    // before it, and none is written.
+    auto wait_prev = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (threadIdx.x == 0 && slots) slots[2 * c].flag = 0;
+        // The merge grid may start now; it waits for this grid's completion.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    };
+    bool ahead = cached;   // planning before the wait
     if (cached) {
         for (int s = threadIdx.x; s < N; s += kThreads) misc->lens[s] = ld_cg(p.seq_lens + s);
         __syncthreads();
-        odd = plan();
-        if (warp == 0 && misc->bnd[1] > misc->bnd[0]) {
-            const Walk w = first_tile();
-            const int fp = w.t * kTile / B;
-            const int pages = (min(kTile, w.L - w.t * kTile) + B - 1) / B;
-            if (lane < pages && fp + lane < p.max_blocks_per_seq && p.num_blocks > 0) {
-                int phys = ld_cg(p.block_tables + static_cast<size_t>(w.s) * p.max_blocks_per_seq + fp + lane);
-                phys = phys < 0 ? 0 : (phys >= p.num_blocks ? p.num_blocks - 1 : phys);
-                tma_prefetch_5d(&tm_k, 0, 0, 0, phys * (B >> 3), w.h);
-                tma_prefetch_5d(&tm_v, 0, 0, 0, phys * (B >> 3), w.h);
-            }
-            if (!MQ && lane < NCH) {
-                const int qx = HP == 2 ? 0 : lane * 64;
-                const int qh = (w.h * HP + (HP == 2 ? lane : 0)) * Gq;
-                tma_prefetch_2d(&tm_q, qx, w.s * H + qh);
-            }
-        }
-    }
-    // Launched as a programmatic dependent of the previous kernel in the
-    // stream: everything above overlaps its tail; apart from L2 prefetches
-    // and reads that are checked below, no global memory is touched before
-    // it has completed.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x == 0 && slots) slots[2 * c].flag = 0;
-    // The merge grid may start now; it waits for this grid's completion.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (cached) {
-        int fresh[kPerMax];
-        int changed = 0;
-#pragma unroll
-        for (int j = 0; j < kPerMax; ++j) {
-            const int s = static_cast<int>(threadIdx.x) + j * kThreads;
-            if (s < N) {
-                fresh[j] = ld_cg(p.seq_lens + s);
-                changed |= fresh[j] != misc->lens[s];
-            }
-        }
-        if (__syncthreads_or(changed)) {
-#pragma unroll
-            for (int j = 0; j < kPerMax; ++j) {
-                const int s = static_cast<int>(threadIdx.x) + j * kThreads;
-                if (s < N) misc->lens[s] = fresh[j];
-            }
-            __syncthreads();
-            odd = plan();
-        }
     } else {
-        odd = plan();
+        wait_prev();
+    }
+    for (;;) {
+        T = plan_range<kThreads>(lens, misc, N, Hkv, c, C, kSegCost, kTileCost, &odd);
+        if (!ahead) break;
+        ahead = false;
+        wait_prev();
+        // Changed values are written back only after every thread has
+        // compared its own (each thread owns the same entries as above).
+        int changed = 0;
+        for (int s = threadIdx.x; s < N; s += kThreads) changed |= ld_cg(p.seq_lens + s) != misc->lens[s];
+        if (!__syncthreads_or(changed)) break;
+        for (int s = threadIdx.x; s < N; s += kThreads) misc->lens[s] = ld_cg(p.seq_lens + s);
+        __syncthreads();
     }
     const int64_t beg = misc->bnd[0], end = misc->bnd[1];
     if (threadIdx.x == 0 && slots) slots[2 * c].range_beg = beg;

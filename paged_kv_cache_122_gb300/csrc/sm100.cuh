@@ -99,34 +99,10 @@ SM100_DEV void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
-// Bring a tensor map's box at the given coordinates into L2 (no
-// shared-memory destination, no barrier).
-SM100_DEV void tma_prefetch_5d(const void *tmap, int c0, int c1, int c2, int c3, int c4) {
-    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];"
-                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-                 : "memory");
-}
-SM100_DEV void tma_prefetch_2d(const void *tmap, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1)
-                 : "memory");
-}
 // Bring `bytes` (a multiple of 16, 16-byte aligned source) into L2.
 SM100_DEV void prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                  : "memory");
-}
-// Bring the 16-byte granules that hold bytes [lo, hi) of `base` into L2, in
-// pieces of at most 64 KiB.  Rounding stays inside the granules of the first
-// and last byte, so no byte outside the pages of the range is touched.
-SM100_DEV void prefetch_l2_span(const void *base, size_t lo, size_t hi) {
-    if (hi <= lo) return;
-    const uint64_t a = (reinterpret_cast<uint64_t>(base) + lo) & ~uint64_t{15};
-    const uint64_t b = (reinterpret_cast<uint64_t>(base) + hi + 15) & ~uint64_t{15};
-    for (uint64_t x = a; x < b; x += 65536u) {
-        const uint64_t n = b - x < 65536u ? b - x : 65536u;
-        prefetch_l2(reinterpret_cast<const void *>(x), static_cast<uint32_t>(n));
-    }
 }
 SM100_DEV void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
