@@ -10,6 +10,24 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Launch as a programmatic dependent of the previous kernel in the stream
+// (the kernels below wait for it before touching memory), so the launch
+// overlaps that kernel's end.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, cudaStream_t stream, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 // One 16-byte vector per thread over the flattened (token, vector) space.
 // A token's K (or V) row, all heads, is contiguous both in the input
 // [T, Hkv, D] and in the cache [P, B, Hkv, D] (flat slot = block * B + offset),
@@ -21,7 +39,10 @@ reshape_and_cache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ 
                          int row_vecs, int64_t num_slots, unsigned int *err) {
     // A decode grid launched as this grid's programmatic dependent may start
     // its set-up now; it reads the cache only after this grid has completed.
+    // This grid is itself a programmatic dependent of the previous kernel in
+    // the stream: it reads and writes nothing before that kernel completed.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t t = i / row_vecs;
     const int e = static_cast<int>(i - t * row_vecs);
@@ -47,6 +68,7 @@ copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                    const int64_t *__restrict__ pairs, int64_t block_vecs, int num_blocks,
                    unsigned int *err) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // as in reshape_and_cache_kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int pair = blockIdx.x;
     const int64_t src = pairs[2 * pair];
     const int64_t dst = pairs[2 * pair + 1];
@@ -85,6 +107,7 @@ reshape_and_cache_layers_kernel(const uint4 *const *k_layers, const uint4 *const
                                 const int64_t *__restrict__ slot_mapping, int num_tokens,
                                 int row_vecs, int64_t num_slots, unsigned int *err) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // as in reshape_and_cache_kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int layer = blockIdx.y;
     const uint4 *k = k_layers[layer];
     const uint4 *v = v_layers[layer];
@@ -114,7 +137,8 @@ __global__ void __launch_bounds__(kThreads)
 copy_blocks_layers_kernel(uint4 *const *k_cache_layers, uint4 *const *v_cache_layers,
                           const int64_t *__restrict__ pairs, int64_t block_vecs, int num_blocks,
                           unsigned int *err) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // as in reshape_and_cache_kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int pair = blockIdx.x;
     const int layer = blockIdx.y >> 1;
     uint4 *c = (blockIdx.y & 1) ? v_cache_layers[layer] : k_cache_layers[layer];
@@ -240,12 +264,12 @@ extern "C" int pk_reshape_and_cache(const void *k, const void *v, void *k_cache,
     if (grid > 0x7fffffff) return PK_ERR_SHAPE;
     unsigned int *err = pk::error_word_ptr();
     if (!err) return PK_ERR_NO_DEVICE;
-    reshape_and_cache_kernel<<<static_cast<unsigned>(grid), kThreads, 0,
-                               reinterpret_cast<cudaStream_t>(stream)>>>(
+    const cudaError_t e = launch_dependent(
+        reshape_and_cache_kernel, dim3(static_cast<unsigned>(grid)), reinterpret_cast<cudaStream_t>(stream),
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(k_cache),
         static_cast<uint4 *>(v_cache), slot_mapping, num_tokens, row_vecs,
         static_cast<int64_t>(num_blocks) * block_size, err);
-    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+    return e == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
 extern "C" int pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
@@ -263,10 +287,11 @@ extern "C" int pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_d
     unsigned int *err = pk::error_word_ptr();
     if (!err) return PK_ERR_NO_DEVICE;
     dim3 grid(static_cast<unsigned>(num_pairs), 2, static_cast<unsigned>(chunks));
-    copy_blocks_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs, block_vecs,
-        num_blocks, err);
-    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+    const cudaError_t e =
+        launch_dependent(copy_blocks_kernel, grid, reinterpret_cast<cudaStream_t>(stream),
+                         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs, block_vecs,
+                         num_blocks, err);
+    return e == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
 namespace {
@@ -292,12 +317,13 @@ extern "C" int pk_reshape_and_cache_layers(const void *const *k_layers, const vo
     if (grid > 0x7fffffff) return PK_ERR_SHAPE;
     unsigned int *err = pk::error_word_ptr();
     if (!err) return PK_ERR_NO_DEVICE;
-    reshape_and_cache_layers_kernel<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(num_layers)),
-                                      kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const uint4 *const *>(k_layers), reinterpret_cast<const uint4 *const *>(v_layers),
-        reinterpret_cast<uint4 *const *>(k_cache_layers), reinterpret_cast<uint4 *const *>(v_cache_layers),
-        slot_mapping, num_tokens, row_vecs, static_cast<int64_t>(num_blocks) * block_size, err);
-    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+    const cudaError_t e = launch_dependent(
+        reshape_and_cache_layers_kernel, dim3(static_cast<unsigned>(grid), static_cast<unsigned>(num_layers)),
+        reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<const uint4 *const *>(k_layers),
+        reinterpret_cast<const uint4 *const *>(v_layers), reinterpret_cast<uint4 *const *>(k_cache_layers),
+        reinterpret_cast<uint4 *const *>(v_cache_layers), slot_mapping, num_tokens, row_vecs,
+        static_cast<int64_t>(num_blocks) * block_size, err);
+    return e == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
 extern "C" int pk_copy_blocks_layers(void *const *k_cache_layers, void *const *v_cache_layers,
@@ -317,10 +343,11 @@ extern "C" int pk_copy_blocks_layers(void *const *k_cache_layers, void *const *v
     unsigned int *err = pk::error_word_ptr();
     if (!err) return PK_ERR_NO_DEVICE;
     dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(2 * num_layers), static_cast<unsigned>(chunks));
-    copy_blocks_layers_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<uint4 *const *>(k_cache_layers), reinterpret_cast<uint4 *const *>(v_cache_layers),
-        src_dst_pairs, block_vecs, num_blocks, err);
-    return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+    const cudaError_t e = launch_dependent(copy_blocks_layers_kernel, grid, reinterpret_cast<cudaStream_t>(stream),
+                                           reinterpret_cast<uint4 *const *>(k_cache_layers),
+                                           reinterpret_cast<uint4 *const *>(v_cache_layers), src_dst_pairs,
+                                           block_vecs, num_blocks, err);
+    return e == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
 extern "C" int pk_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
