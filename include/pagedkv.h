@@ -221,6 +221,36 @@ int pk_selftest_decode_wait_timeout(void *out, int out_dtype, const void *q,
                                     pk_stream_t stream);
 
 /*
+ * Self-test of the length check after the programmatic wait; the pages have
+ * no counterpart.
+ *
+ * The tensor-core decode kernel is launched as a programmatic dependent of
+ * the previous kernel in the stream.  With num_seqs <= 2048 it copies the
+ * sequence lengths into shared memory and plans its range of the work before
+ * that kernel has completed, then reads the lengths again after the wait and
+ * plans again if any differs (the previous kernel may have written them).
+ * This call runs pk_paged_attention_decode on the tensor-core kernel with the
+ * first read taken from `stale_seq_lens` instead of `seq_lens`, so that the
+ * second plan, from `seq_lens`, is the one used whenever the two differ.  The
+ * result must equal that of pk_paged_attention_decode with the same inputs.
+ *
+ *   stale_seq_lens  [num_seqs] int32 DEVICE array, any values (lengths outside
+ *                   [0, max_seq_len] included: only seq_lens is checked and
+ *                   reported); unused when num_seqs > 2048
+ *   everything else as for pk_paged_attention_decode.
+ * Returns PK_ERR_NULL if stale_seq_lens is NULL.
+ */
+int pk_selftest_decode_stale_lengths(void *out, int out_dtype, const void *q,
+                                     const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *seq_lens, int max_seq_len,
+                                     int num_seqs, int num_heads, int num_kv_heads,
+                                     int head_dim, int num_blocks, int block_size,
+                                     float scale, const int32_t *stale_seq_lens,
+                                     void *workspace, size_t workspace_bytes,
+                                     pk_stream_t stream);
+
+/*
  * Attention of SEVERAL new tokens per sequence over the paged cache, causal
  * among them: chunked prefill of a prompt ("PagedAttention from First
  * Principles", §12) and speculative-decoding verification, where the

@@ -28,6 +28,7 @@ from .api import (  # noqa: F401
     pk_reshape_and_cache,
     pk_reshape_and_cache_layers,
     pk_selftest_decode_wait_timeout,
+    pk_selftest_decode_stale_lengths,
     pk_set_decode_path,
     pk_swap_blocks,
     reshape_and_cache,

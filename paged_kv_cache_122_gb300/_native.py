@@ -32,6 +32,10 @@ SIGNATURES = {
         c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
         c_int, c_int, c_int, c_int, c_int, c_int, c_float,
         c_void_p, c_size_t, c_int, c_uint, c_void_p]),   # workspace, bytes, stall_tile, wait_limit_us, stream
+    "pk_selftest_decode_stale_lengths": (c_int, [
+        c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
+        c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+        c_void_p, c_void_p, c_size_t, c_void_p]),       # stale_seq_lens, workspace, bytes, stream
     "pk_paged_attention_multi_query": (c_int, [
         c_void_p, c_int, c_void_p, c_int,      # out, out_dtype, q, total_q
         c_void_p, c_int,                       # cu_q_lens, max_q_len

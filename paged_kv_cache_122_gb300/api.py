@@ -127,6 +127,25 @@ def pk_selftest_decode_wait_timeout(out: torch.Tensor, q: torch.Tensor, k_cache:
             _stream(dev, stream)))
 
 
+def pk_selftest_decode_stale_lengths(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                     v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                     scale: float, max_seq_len: int, stale_seq_lens: torch.Tensor,
+                                     workspace: torch.Tensor, stream=None) -> int:
+    """Self-test of the length check after the programmatic wait (see the C
+    header): a decode call on the tensor-core kernel that plans first from
+    ``stale_seq_lens`` and must plan again from ``seq_lens``.  Returns the
+    call's status."""
+    dev = q.device
+    N, H, D = q.shape
+    P, B, Hkv, _ = k_cache.shape
+    with torch.cuda.device(dev):
+        return int(load().pk_selftest_decode_stale_lengths(
+            _ptr(out), _native.PK_FP32 if out.dtype == torch.float32 else _native.PK_BF16, _ptr(q),
+            _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+            int(max_seq_len), N, H, Hkv, D, P, B, float(scale), _ptr(stale_seq_lens), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+
+
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                            block_size: Optional[int] = None, *, out_dtype=torch.bfloat16,

@@ -34,6 +34,10 @@ struct DecodeParams {
     // Self-test of the bounded waits: when > 0, CTA 0's producer issues no
     // copy from this tile of its range on, so its consumers' waits run out.
     int stall_tile;
+    // The lengths the tensor-core kernel plans from before the programmatic
+    // wait (NULL = seq_lens).  After the wait it reads seq_lens and redoes the
+    // plan if they differ; the self-test of that check passes other values.
+    const int32_t *lens_ahead;
     // Multi-query attention (tensor-core path): q is [total_q, H, D] and
     // sequence s owns query rows cu_q_lens[s] .. cu_q_lens[s+1]-1, its newest
     // tokens, causal among themselves; q_len is the padded number of query

@@ -48,13 +48,14 @@ extern "C" int pk_set_decode_path(int path) {
 namespace {
 
 // The decode call; `stall_tile` and `wait_limit_ns` serve the self-test of
-// the bounded waits (0 = off / the default limit), which also forces the
-// tensor-core kernel.
+// the bounded waits (0 = off / the default limit) and `lens_ahead` the
+// self-test of the length check after the programmatic wait (NULL = off);
+// either forces the tensor-core kernel.
 int decode_impl(void *out, int out_dtype, const void *q, const void *k_cache, const void *v_cache,
                 const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens, int max_seq_len,
                 int num_seqs, int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
                 float scale, void *workspace, size_t workspace_bytes, pk_stream_t stream, int stall_tile,
-                uint64_t wait_limit_ns) {
+                uint64_t wait_limit_ns, const int32_t *lens_ahead) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
         max_blocks_per_seq < 0 || max_seq_len < 0 || block_size <= 0)
         return PK_ERR_SHAPE;
@@ -92,7 +93,8 @@ int decode_impl(void *out, int out_dtype, const void *q, const void *k_cache, co
     p.scale_log2 = scale * pk::kLog2e;
     p.stall_tile = stall_tile;
     p.wait_limit_ns = wait_limit_ns;
-    const int path = stall_tile > 0 ? PK_PATH_TENSOR_CORE : g_path.load();
+    p.lens_ahead = lens_ahead;
+    const int path = (stall_tile > 0 || lens_ahead) ? PK_PATH_TENSOR_CORE : g_path.load();
     const int G = num_heads / num_kv_heads;
     // A batch whose 128-token tiles could not give every SM even one (at most
     // num_seqs * Hkv * ceil(max_seq_len / 128) of them) is bound by launch
@@ -146,7 +148,7 @@ extern "C" int pk_paged_attention_decode(void *out, int out_dtype, const void *q
                                          pk_stream_t stream) {
     return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
-                       workspace, workspace_bytes, stream, 0, 0);
+                       workspace, workspace_bytes, stream, 0, 0, nullptr);
 }
 
 extern "C" int pk_selftest_decode_wait_timeout(void *out, int out_dtype, const void *q,
@@ -160,7 +162,22 @@ extern "C" int pk_selftest_decode_wait_timeout(void *out, int out_dtype, const v
     if (stall_tile < 1 || wait_limit_us < 100 || wait_limit_us > 1000000) return PK_ERR_SHAPE;
     return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                        max_seq_len, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
-                       workspace, workspace_bytes, stream, stall_tile, static_cast<uint64_t>(wait_limit_us) * 1000u);
+                       workspace, workspace_bytes, stream, stall_tile, static_cast<uint64_t>(wait_limit_us) * 1000u,
+                       nullptr);
+}
+
+extern "C" int pk_selftest_decode_stale_lengths(void *out, int out_dtype, const void *q,
+                                                const void *k_cache, const void *v_cache,
+                                                const int32_t *block_tables, int max_blocks_per_seq,
+                                                const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                                                int num_heads, int num_kv_heads, int head_dim,
+                                                int num_blocks, int block_size, float scale,
+                                                const int32_t *stale_seq_lens, void *workspace,
+                                                size_t workspace_bytes, pk_stream_t stream) {
+    if (!stale_seq_lens) return PK_ERR_NULL;
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                       max_seq_len, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                       workspace, workspace_bytes, stream, 0, 0, stale_seq_lens);
 }
 
 extern "C" int pk_paged_attention_multi_query(void *out, int out_dtype, const void *q, int total_q,

@@ -387,7 +387,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     };
     bool ahead = cached;   // planning before the wait
     if (cached) {
-        for (int s = threadIdx.x; s < N; s += kThreads) misc->lens[s] = ld_cg(p.seq_lens + s);
+        const int32_t *ahead = p.lens_ahead ? p.lens_ahead : p.seq_lens;
+        for (int s = threadIdx.x; s < N; s += kThreads) misc->lens[s] = ld_cg(ahead + s);
         __syncthreads();
     } else {
         wait_prev();

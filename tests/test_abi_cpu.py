@@ -123,6 +123,22 @@ def test_selftest_host_validation(lib):
         assert call() == -7
 
 
+def test_stale_lengths_selftest_host_validation(lib):
+    f = lib.pk_selftest_decode_stale_lengths
+
+    def call(**kw):
+        a = dict(out=_fake(), dt=0, q=_fake(), kc=_fake(), vc=_fake(), bt=_fake(), mb=4, sl=_fake(), msl=64,
+                 n=2, h=8, hkv=2, d=128, nb=16, b=16, scale=0.088, stale=_fake(), ws=_fake(), wsb=1 << 30)
+        a.update(kw)
+        return f(a["out"], a["dt"], a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"], a["msl"], a["n"], a["h"],
+                 a["hkv"], a["d"], a["nb"], a["b"], a["scale"], a["stale"], a["ws"], a["wsb"], None)
+    assert call(stale=NULL) == -1                             # the stale lengths are required
+    assert call(d=96) == -3                                   # then the decode call's own checks
+    assert call(n=0) == 0
+    if not torch.cuda.is_available():
+        assert call() == -7
+
+
 def test_cache_ops_host_validation(lib):
     f = lib.pk_reshape_and_cache
     assert f(_fake(), _fake(), _fake(), _fake(), _fake(), 4, 8, 100, 16, 16, None) == -3
