@@ -9,9 +9,9 @@
 // its reduce step).
 //
 // Work split.  The flattened space (sequence, KV head, 128-token tile) is cut
-// into gridDim.x contiguous ranges of equal cost (a tile costs kTileCost, a
-// (sequence, head) segment kSegCost more), one per persistent CTA (one CTA
-// per SM).  A CTA's range covers whole segments, which it writes straight to
+// into gridDim.x contiguous ranges of equal cost (tiles, tokens and
+// (sequence, head) segments each weighted; see kTileCost), one per
+// persistent CTA (one CTA per SM).  A CTA's range covers whole segments, which it writes straight to
 // the output, plus at most two cut segments at its ends, whose partial (max,
 // denominator, unnormalised output) go to a workspace slot and are combined
 // by the merge kernel.
@@ -164,18 +164,25 @@ struct Walk {
     }
 };
 
-// This CTA's range of the flattened tile space.  Tile x (its cost interval
-// starting at a_x: a segment's tile 0 covers [start, start + seg_cost +
-// kTileCost), tile t >= 1 starts at start + seg_cost + kTileCost * t)
-// belongs to CTA k when P_k <= a_x < P_{k+1}, P_k = k * W / C, W the total
-// cost.  Writes misc->bnd (the first tile of this range and of the next),
+// This CTA's range of the flattened tile space.  Tile x, whose cost interval
+// starts at a_x (a segment's tile 0 at its start, tile t >= 1 at start +
+// seg_cost + full * t, full the cost of a full tile), belongs to CTA k when
+// P_k <= a_x < P_{k+1}, P_k = k * W / C, W the total cost.  Writes misc->bnd (the first tile of this range and of the next),
 // misc->s0 / rem0 (where the range starts) and misc->first_cta (the CTA in
 // whose range a segment cut at this range's start begins); returns the
 // total tile count and, in *odd, whether some length is zero or outside
 // [0, cap] (the same for every thread).  Every thread of the CTA calls it.
 template <int kThreadsT, typename MiscT>
 __device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, int N, int Hkv, int c, int C,
-                                           int64_t seg_cost, int tile_cost, int *odd) {
+                                           int64_t seg_cost, int tile_cost, int tok_cost, int *odd) {
+    // A segment of L tokens in nt tiles costs seg_cost + tile_cost * nt -
+    // tok_cost * L: a full tile costs full = tile_cost - tok_cost * kTile, and
+    // only a segment's last tile can be partial, so tile t >= 1 starts at
+    // seg_cost + full * t.
+    const int64_t full = tile_cost - static_cast<int64_t>(tok_cost) * kTile;
+    auto seg_total = [&](int64_t nt, int L) -> int64_t {
+        return nt > 0 ? seg_cost + tile_cost * nt - static_cast<int64_t>(tok_cost) * L : 0;
+    };
     const int per = (N + kThreadsT - 1) / kThreadsT;
     const int s_lo = min(N, static_cast<int>(threadIdx.x) * per), s_hi = min(N, s_lo + per);
     const int cap = lens.cap;
@@ -184,9 +191,10 @@ __device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, in
     for (int s = s_lo; s < s_hi; ++s) {
         const int raw = lens.raw(s);
         bad |= raw <= 0 || raw > cap;
-        const int64_t nt = (lens(s) + kTile - 1) / kTile;
+        const int L = lens(s);
+        const int64_t nt = (L + kTile - 1) / kTile;
         mine += nt * Hkv;
-        mine_w += nt > 0 ? (tile_cost * nt + seg_cost) * Hkv : 0;
+        mine_w += seg_total(nt, L) * Hkv;
     }
     int64_t T, W;
     const int64_t my_off = block_exclusive_scan<kThreadsT>(mine, misc->scan, &T);
@@ -200,15 +208,16 @@ __device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, in
         if (my_off_w <= P && P < my_off_w + mine_w) {
             int64_t acc_t = my_off, acc_w = my_off_w;
             for (int s = s_lo; s < s_hi; ++s) {
-                const int64_t nt = (lens(s) + kTile - 1) / kTile;
-                const int64_t segc = tile_cost * nt + seg_cost;
-                const int64_t cw = nt > 0 ? segc * Hkv : 0;
+                const int L = lens(s);
+                const int64_t nt = (L + kTile - 1) / kTile;
+                const int64_t segc = seg_total(nt, L);
+                const int64_t cw = segc * Hkv;
                 if (P < acc_w + cw) {
                     const int64_t q = P - acc_w;
                     int64_t h = q / segc;
                     const int64_t r = q - h * segc;
                     // The first tile of the segment that starts at or after r.
-                    int64_t t = r == 0 ? 0 : (r - seg_cost + tile_cost - 1) / tile_cost;
+                    int64_t t = r == 0 ? 0 : (r - seg_cost + full - 1) / full;
                     if (r > 0 && t < 1) t = 1;
                     if (t >= nt) {
                         ++h;
@@ -228,7 +237,8 @@ __device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, in
         int64_t acc = my_off, acc_w = my_off_w;
         if (acc <= b0 && b0 < acc + mine) {
             for (int s = s_lo; s < s_hi; ++s) {
-                const int64_t nt = (lens(s) + kTile - 1) / kTile;
+                const int L = lens(s);
+                const int64_t nt = (L + kTile - 1) / kTile;
                 const int64_t w = nt * Hkv;
                 if (b0 < acc + w) {
                     misc->s0 = s;
@@ -236,7 +246,7 @@ __device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, in
                     // If the range starts inside a segment, the CTA where that
                     // segment starts (the owner of its tile 0's cost start).
                     const int64_t h0 = (b0 - acc) / nt;
-                    const int64_t a = acc_w + h0 * (tile_cost * nt + seg_cost);
+                    const int64_t a = acc_w + h0 * seg_total(nt, L);
                     int64_t k = W > 0 ? a * C / W : 0;
                     while (k + 1 < C && (k + 1) * W / C <= a) ++k;
                     while (k > 0 && k * W / C > a) --k;
@@ -244,7 +254,7 @@ __device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, in
                     break;
                 }
                 acc += w;
-                acc_w += nt > 0 ? (tile_cost * nt + seg_cost) * Hkv : 0;
+                acc_w += seg_total(nt, L) * Hkv;
             }
         }
     }
@@ -253,15 +263,22 @@ __device__ __forceinline__ int64_t plan_range(const LenSrc lens, MiscT *misc, in
 }
 
 // The flattened (sequence, KV head, tile) space is cut into ranges of equal
-// cost, not of equal tile count: a CTA's time grows with the (sequence,
-// KV head) segments in its range (each loads its queries, sets up and reads
-// out its O) as well as with its tiles.  Measured per CTA with in-kernel
-// timestamps on the Llama-3-70B length mix: a segment costs about 0.36 of a
-// tile when at most 8 query columns are in use, and about 1.4 tiles with 16
-// (the read-out and the reference-max moves work on every column).
-constexpr int64_t kTileCost = 7;
-template <int NUSED>
-constexpr int64_t seg_cost() { return NUSED > 8 ? 10 : 2; }
+// cost, not of equal tile count.  A segment of L tokens in nt tiles costs
+// seg_cost + kTileCost * nt - kTokCost * L: a CTA's time grows with its
+// (sequence, KV head) segments (each loads its queries, sets up and reads
+// out its O) and with its tiles, and a tile's time shrinks less than its
+// bytes when it is only partly filled (the ring holds a fixed number of
+// tiles, so a partial tile keeps fewer bytes in flight).  The weights come
+// from a least-squares fit of per-CTA times (in-kernel timestamps) to the
+// tiles, pages and segments of each CTA's range, over back-to-back calls on
+// five batches: a full tile costs 272, a one-token tile 399, a segment 56 --
+// 200 when 16 query columns are in use (the read-out and the reference-max
+// moves work on every column) -- and half as much with head pairs, whose
+// tiles carry twice the bytes.
+constexpr int64_t kTileCost = 400;
+constexpr int kTokCost = 1;
+template <int NUSED, int HP>
+constexpr int64_t seg_cost() { return (NUSED > 8 ? 200 : 56) / HP; }
 
 // Warp max of a float in one integer reduction: the bits are mapped to an
 // unsigned key with the same order (a non-negative float gets its sign bit
@@ -305,7 +322,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     constexpr uint32_t kTmemCols = HP == 2 ? 128 : 64;
     constexpr int CW = HP == 2 ? 8 : kNPad;           // P columns per head of the tile
     constexpr int NCOL = HP == 2 ? 8 + NC : NC;       // columns 0 .. NCOL-1 may be in use
-    constexpr int64_t kSegCost = seg_cost<HP * NC>();   // a segment's cost (the columns in use), in 1/7 tiles
+    constexpr int64_t kSegCost = seg_cost<HP * NC, HP>();   // a segment's cost (the columns in use, head pairs)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -394,7 +411,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         wait_prev();
     }
     for (;;) {
-        T = plan_range<kThreads>(lens, misc, N, Hkv, c, C, kSegCost, kTileCost, &odd);
+        T = plan_range<kThreads>(lens, misc, N, Hkv, c, C, kSegCost, kTileCost, kTokCost, &odd);
         if (!ahead) break;
         ahead = false;
         wait_prev();
@@ -922,9 +939,9 @@ __global__ void __launch_bounds__(128)
 decode_tc_merge_kernel(const DecodeParams p, int C) {
     constexpr int CW = HP == 2 ? 8 : kNPad;
     // A decode grid launched next in the stream as this grid's programmatic
-    // dependent may begin its set-up (it touches no global memory but L2
-    // prefetches before this grid completes).  Its CTAs find room only as
-    // this decode grid's CTAs leave their SMs.
+    // dependent may begin its set-up (before this grid completes it reads
+    // only the sequence lengths, and reads them again afterwards).  Its CTAs
+    // find room only as this decode grid's CTAs leave their SMs.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the decode grid: wait for it
     // to finish and its writes to be visible.
