@@ -67,3 +67,44 @@ def test_stale_lengths_give_the_normal_result(name, kind):
         ref = oracle.paged_decode_attention(host_bits(t["q"]), host_bits(t["k_cache"]), host_bits(t["v_cache"]),
                                             w.block_tables, w.seq_lens, w.scale, w.block_size)
         assert_close(out.cpu().numpy(), ref, False, "decode planned from stale lengths")
+
+
+@pytest.mark.parametrize("stale", ["ones", "reversed"])
+def test_lengths_written_by_the_previous_kernel(stale):
+    """The kernel before the decode call writes the lengths: here
+    reshape_and_cache, whose cache rows alias the lengths array (one KV head
+    of 64 elements = 32 int32 per slot), itself delayed behind a long fill.
+    The decode grid is launched as that kernel's programmatic dependent, so
+    it may read the lengths before they are written; its result must be that
+    of the new lengths."""
+    w = W.get("l3-8b", 2)
+    t = W.make_tensors(w, DEV)
+    n = w.num_seqs
+    rows = (n * 4 + 127) // 128                       # 128-byte slots holding the lengths
+    lens_cache = torch.zeros((1, 16, 1, 64), dtype=torch.bfloat16, device=DEV)
+    dummy_v = torch.zeros_like(lens_cache)
+    lens_view = lens_cache.view(-1).view(torch.int32)[:n]
+    old = w.seq_lens.astype(np.int32)
+    lens_view.copy_(torch.from_numpy(np.ones(n, np.int32) if stale == "ones" else np.ascontiguousarray(old[::-1])))
+    new_rows = np.zeros(rows * 32, np.int32)
+    new_rows[:n] = old
+    k_new = torch.from_numpy(new_rows.view(np.int16).copy()).view(torch.bfloat16).view(rows, 1, 64).to(DEV)
+    v_new = torch.zeros_like(k_new)
+    slots = torch.arange(rows, dtype=torch.int64, device=DEV)
+    ws = pk.new_workspace(pk.pk_decode_workspace_bytes(n, w.num_heads, w.num_kv_heads, w.head_dim, w.max_seq_len), DEV)
+    big = torch.empty(1 << 30, dtype=torch.uint8, device=DEV)
+    ref = oracle.paged_decode_attention(host_bits(t["q"]), host_bits(t["k_cache"]), host_bits(t["v_cache"]),
+                                        w.block_tables, w.seq_lens, w.scale, w.block_size)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        lens_view.copy_(torch.from_numpy(np.ones(n, np.int32) if stale == "ones" else np.ascontiguousarray(old[::-1])))
+        torch.cuda.synchronize()
+        big.fill_(1)                                   # keeps the append waiting
+        pk.reshape_and_cache(k_new, v_new, lens_cache, dummy_v, slots)
+        got = pk.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], lens_view,
+                                        w.scale, w.block_size, out_dtype=torch.float32,
+                                        max_seq_len=w.max_seq_len, workspace=ws)
+        torch.cuda.synchronize()
+        assert pk.pk_get_device_error() == 0
+        assert np.array_equal(lens_view.cpu().numpy(), old)
+        assert_close(got.cpu().numpy(), ref, False, "decode after the lengths were written by the previous kernel")
