@@ -1052,7 +1052,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-// K or V pages: one box per (page, group of HP adjacent KV heads) holding
+// K or V pages (L2 fetches the 128-byte pieces the box is made of: with
+// 256-byte promotion the calls took 0.3 % longer) -- one box per (page,
+// group of HP adjacent KV heads) holding
 // its B rows as B / 8 blocks of 8 rows, each block [chunk][8 rows][64] in
 // shared memory (dimensions: 64 elements; row within the block; 128-byte
 // chunk of the group's row -- a 64-element half of the head, or (HP = 2,
@@ -1068,7 +1070,7 @@ bool encode_page_map(CUtensorMap *m, const void *base, const DecodeParams &p, in
     cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(D * HP / 64), static_cast<cuuint32_t>(B / 8), 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
