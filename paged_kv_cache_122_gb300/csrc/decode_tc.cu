@@ -404,8 +404,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     };
     bool ahead = cached;   // planning before the wait
     if (cached) {
-        const int32_t *ahead = p.lens_ahead ? p.lens_ahead : p.seq_lens;
-        for (int s = threadIdx.x; s < N; s += kThreads) misc->lens[s] = ld_cg(ahead + s);
+        const int32_t *first_read = p.lens_ahead ? p.lens_ahead : p.seq_lens;
+        for (int s = threadIdx.x; s < N; s += kThreads) misc->lens[s] = ld_cg(first_read + s);
         __syncthreads();
     } else {
         wait_prev();
